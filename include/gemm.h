@@ -1,0 +1,163 @@
+/*
+ * gemm.h -- C ABI of libgemm.so, the GB300 (sm_103a) software-pipelined GEMM.
+ *
+ * Operation (every entry point below):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * The problem is the tiled GEMM of "CUTLASS-CuTe 初步(6)" (hxf0223.github.io),
+ * section 2 "Thread Block Tile": each thread block owns one tile of C and loops
+ * over K, accumulating the product of an A tile and a B tile per step.  The
+ * page's own formula was lost; the BLAS form with alpha and beta is used.
+ * What the library adds is the mainloop the four pages describe: the next K
+ * tile's global-to-shared copy overlaps the current tile's multiply-accumulate
+ * through a ring of `stages` shared-memory buffers ("learn-kernels.com,
+ * Matrix multiplication", the paragraph "Overlap needs stages"; "Software
+ * Pipelining and Double Buffering", sections "Double buffering with shared
+ * memory" and "Multi-stage pipelines").  stages = 1 is the single buffer with
+ * a load phase and a compute phase per K tile, stages = 2 is double
+ * buffering, stages >= 3 is a multi-stage ring.  The stage count changes
+ * timing only: for one dtype and tile, every stage count gives bit-identical C.
+ *
+ * Layout (all row-major, leading dimensions in elements):
+ *   A  M x K, element (i,k) at A[i*lda + k], lda >= K
+ *   B  K x N, row-major: element (k,j) at B[k*ldb + j], ldb >= N
+ *           column-major (gemm_ex, b_col_major = 1): B[j*ldb + k], ldb >= K
+ *   C  M x N, element (i,j) at C[i*ldc + j], ldc >= N
+ *
+ * Types (`dtype`, input -> output; accumulation is always fp32):
+ *   GEMM_F32        fp32 A, B, C      CUDA-core SIMT sgemm, stages 1..4
+ *   GEMM_F16_F32    fp16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
+ *   GEMM_BF16_F32   bf16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
+ *   GEMM_BF16_BF16  bf16 A, B, C      tcgen05 tensor cores, stages 1..6;
+ *                                     fp32 result rounded to nearest even
+ *   alpha and beta are fp32.  alpha is applied to the fp32 sum, then beta*C
+ *   is added (one fp32 multiply-add per element).
+ *
+ * Memory: A, B and C are device pointers owned by the caller (except in
+ * gemm_host, which takes host pointers).  The library keeps no pointer after
+ * a call returns.
+ *
+ * Alignment (GEMM_ERR_ALIGN otherwise): A, B and C start on 16-byte
+ * boundaries and lda*size, ldb*size and ldc*size are multiples of 16 bytes
+ * (size = element size of that operand).  These are the tensor-copy (TMA)
+ * and 16-byte cp.async rules; there is no slower fallback path.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * gemm and gemm_ex enqueue work and return without synchronising.
+ *
+ * Degenerate sizes: M == 0 or N == 0 does nothing.  K == 0 or alpha == 0
+ * gives C = beta*C without reading A or B.  beta == 0 never reads C (so NaN
+ * in C does not propagate), following the BLAS convention.
+ *
+ * Error behaviour: every entry point returns a gemm_status_t.  Argument
+ * checks happen on the host before anything is enqueued.  Inside the
+ * tensor-core kernel every wait on a pipeline barrier is bounded in time; a
+ * wait that runs out records GEMM_ERR_TIMEOUT in a device status word and the
+ * kernel returns early (its output is then undefined).  gemm and gemm_ex do
+ * not look at that word (they would have to synchronise); gemm_checked does.
+ */
+#ifndef SSP_GEMM_H
+#define SSP_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_F32 = 0,
+    GEMM_F16_F32 = 1,
+    GEMM_BF16_F32 = 2,
+    GEMM_BF16_BF16 = 3
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_ARG = -1,          /* bad size, leading dimension, pointer, dtype or stages */
+    GEMM_ERR_UNSUPPORTED = -2,  /* a valid request this build does not implement */
+    GEMM_ERR_ALIGN = -3,        /* a 16-byte alignment rule above is broken */
+    GEMM_ERR_LAUNCH = -4,       /* the CUDA launch (or tensor-map encode) failed */
+    GEMM_ERR_TIMEOUT = -5,      /* a pipeline wait ran out (gemm_checked only) */
+    GEMM_ERR_CUDA = -6          /* another CUDA runtime call failed (copies, sync, device) */
+} gemm_status_t;
+
+/*
+ * gemm -- C = alpha*A*B + beta*C with row-major B, asynchronous on `stream`.
+ *   M, N, K    problem size (>= 0)
+ *   A, lda     device pointer and leading dimension of A (M x K)
+ *   B, ldb     device pointer and leading dimension of B (K x N, row-major)
+ *   C, ldc     device pointer and leading dimension of C (M x N), read when
+ *              beta != 0 and written
+ *   dtype      a gemm_dtype_t
+ *   stages     depth of the shared-memory ring: 1..6 on the tensor-core path,
+ *              1..4 on the SIMT path
+ *   stream     cudaStream_t
+ * The tensor-core tile is 128 x 256 for stages <= 4 and 128 x 128 above.
+ */
+int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+         void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, void* stream);
+
+/*
+ * gemm_ex -- gemm with two more choices.
+ *   b_col_major  0: B row-major (as gemm); 1: B column-major (element (k,j)
+ *                at B[j*ldb + k], ldb >= K).  Column-major B is implemented on
+ *                the tensor-core path only (GEMM_ERR_UNSUPPORTED for GEMM_F32).
+ *   tile_n       tensor-core tile width: 0 = the gemm default, 128 or 256.
+ *                128 allows stages 1..6, 256 allows stages 1..4 (shared-memory
+ *                capacity).  Must be 0 on the SIMT path (its tile is 128 x 64).
+ */
+int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+            int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
+            int b_col_major, int tile_n, void* stream);
+
+/*
+ * gemm_checked -- gemm_ex, then synchronise `stream` and read (and clear) the
+ * device status word.  Returns GEMM_ERR_TIMEOUT if a pipeline wait ran out,
+ * GEMM_ERR_CUDA if the stream reported an error, otherwise gemm_ex's status.
+ * Meant for tests and debugging; it blocks the calling thread.
+ */
+int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                 int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype,
+                 int stages, int b_col_major, int tile_n, void* stream);
+
+/*
+ * gemm_host -- the same operation on HOST buffers: copies A, B (and C when
+ * beta != 0) to the device, runs gemm_ex on `stream`, copies C back and
+ * synchronises.  Device staging buffers are allocated on first use and
+ * cached per device (grown when a larger problem arrives); pinned host memory
+ * makes the copies asynchronous DMA.  Leading dimensions are kept as given.
+ */
+int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+              int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
+              int b_col_major, int tile_n, void* stream);
+
+/* Frees gemm_host's cached device buffers on the current device. */
+int gemm_host_release(void);
+
+/* Human-readable name of a gemm_status_t (static storage). */
+const char* gemm_status_string(int status);
+
+/* Largest `stages` value accepted for a dtype and tile_n (as in gemm_ex), or
+ * GEMM_ERR_ARG for an unknown combination. */
+int gemm_max_stages(int dtype, int tile_n);
+
+/*
+ * gemm_debug_set -- test hook for the bounded waits (not thread-safe; affects
+ * later launches of the tensor-core kernel from this process).
+ *   wait_limit_ns      time a pipeline wait may spin before it gives up
+ *                      (<= 0 restores the default of 2 s)
+ *   withhold_arrive    -1: normal.  k >= 0: block 0's producer skips the
+ *                      copy and the barrier arrive of its k-th K tile, so the
+ *                      MMA warp's wait on that stage runs out.  Used to check
+ *                      that a stuck pipeline ends with GEMM_ERR_TIMEOUT
+ *                      instead of a hang.
+ */
+int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSP_GEMM_H */

@@ -1,0 +1,65 @@
+// internal.h -- launcher interfaces shared by the C ABI (gemm_api.cu) and the
+// two kernels (gemm_tc_sm103a.cu, sgemm_simt.cu).  Not installed; the public
+// interface is include/gemm.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ssp {
+
+// Device status word written by a pipeline wait that ran out.
+struct GemmDeviceStatus {
+    int code;   // 0 = fine, else GEMM_ERR_TIMEOUT
+    int block;  // blockIdx.x of the first CTA that gave up
+    int role;   // 0 producer, 1 MMA issuer, 2 epilogue
+    int iter;   // the K-tile iteration (producer/MMA) or tile count (epilogue)
+};
+
+struct TcLaunch {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    void* C;
+    int64_t ldc;
+    float alpha, beta;
+    int in_bf16;      // 0 fp16 inputs, 1 bf16 inputs
+    int out_bf16;     // 0 fp32 output, 1 bf16 output
+    int b_col_major;  // 0 B row-major (N contiguous), 1 B column-major (K contiguous)
+    int stages;       // 1..6
+    int tile_n;       // 128 or 256
+    int64_t wait_limit_ns;
+    int withhold_arrive;
+};
+
+struct SimtLaunch {
+    int64_t M, N, K;
+    const float* A;
+    int64_t lda;
+    const float* B;
+    int64_t ldb;
+    float* C;
+    int64_t ldc;
+    float alpha, beta;
+    int stages;  // 1..4
+};
+
+// Enqueue the tensor-core GEMM (K > 0, M > 0, N > 0, alpha != 0).  Returns a
+// gemm_status_t.
+int tc_launch(const TcLaunch& L, cudaStream_t stream);
+// Read the device status word of the tensor-core kernel on the current device
+// and reset it to zero (synchronous).
+int tc_read_and_clear_status(GemmDeviceStatus* out);
+
+int simt_launch(const SimtLaunch& L, cudaStream_t stream);
+
+// C = beta*C over an M x N block (K == 0 or alpha == 0); elem_bytes 4 (fp32) or 2 (bf16).
+int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,
+                 cudaStream_t stream);
+
+constexpr int kTcMaxStages128 = 6;
+constexpr int kTcMaxStages256 = 4;
+constexpr int kSimtMaxStages = 4;
+
+}  // namespace ssp

@@ -1,0 +1,266 @@
+// sgemm_simt.cu -- FP32 CUDA-core GEMM with cp.async staging, 1..4 stages.
+//
+// The register-blocked sgemm the pages treat as the FP32 path: a 128 x 64
+// block tile, 128 threads, each thread accumulating an 8 x 8 tile of C as the
+// outer product of an 8 x 1 A fragment and a 1 x 8 B fragment per k
+// ("CUTLASS-CuTe 初步(6)", section 4 "Thread Tile"; the CUDA Handbook's
+// chapter 17 register-blocked 128 x 64 kernel).  Tiles go global -> shared with
+// 16-byte cp.async (no register staging, "learn-kernels.com, Matrix
+// multiplication", paragraph on LDGSTS), one commit group per stage.
+//
+// stages = 1 is the single-buffer loop with two barriers per K tile (load,
+// barrier, compute, barrier: "CUTLASS-CuTe 初步(6)" section 6.2, first loop).
+// stages >= 2 keeps S-1 tiles in flight: at the top of each iteration it
+// waits until at most S-2 groups are pending, then one barrier (which both
+// publishes the landed tile and proves every thread is done with the slot
+// about to be refilled), then issues the copy S-1 tiles ahead and computes --
+// one barrier per iteration, as the pages' double-buffered loops have.
+// Out-of-range rows/columns are zero-filled by cp.async's source-size operand,
+// so ragged M, N and K need no special path; stores are masked.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ssp {
+namespace {
+
+constexpr int BM = 128, BN = 64, BK = 16;
+constexpr int THREADS = 128;
+constexpr int A_LD = BK + 4;  // padded row (80 bytes): conflict-free fragment reads
+constexpr int A_STAGE_FLOATS = BM * A_LD;
+constexpr int B_STAGE_FLOATS = BK * BN;
+
+struct SimtParams {
+    int M, N, K;
+    const float* A;
+    long long lda;
+    const float* B;
+    long long ldb;
+    float* C;
+    long long ldc;
+    float alpha, beta;
+};
+
+// Copy K tile kt into stage buffers (As, Bs).  A tile: 128 rows x 16 floats =
+// 512 16-byte chunks; B tile: 16 rows x 64 floats = 256 chunks.
+__device__ __forceinline__ void load_tile(const SimtParams& p, int m0, int n0, int kt, float* As,
+                                          float* Bs) {
+    const int tid = threadIdx.x;
+    const int k0 = kt * BK;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int c = tid + THREADS * i;
+        const int row = c >> 2;
+        const int kc = (c & 3) * 4;
+        const int gm = m0 + row, gk = k0 + kc;
+        int valid = 0;
+        const float* src = p.A;
+        if (gm < p.M && gk < p.K) {
+            valid = min(p.K - gk, 4) * 4;
+            src = p.A + static_cast<long long>(gm) * p.lda + gk;
+        }
+        cp_async_16(smem_addr(As + row * A_LD + kc), src, static_cast<uint32_t>(valid));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c = tid + THREADS * i;
+        const int row = c >> 4;
+        const int nc = (c & 15) * 4;
+        const int gk = k0 + row, gn = n0 + nc;
+        int valid = 0;
+        const float* src = p.B;
+        if (gk < p.K && gn < p.N) {
+            valid = min(p.N - gn, 4) * 4;
+            src = p.B + static_cast<long long>(gk) * p.ldb + gn;
+        }
+        cp_async_16(smem_addr(Bs + row * BN + nc), src, static_cast<uint32_t>(valid));
+    }
+}
+
+// acc[r][j] += A[ty + 16 r][k] * B[k][col(j)] over the BK values of one stage.
+// Thread rows are ty, ty+16, ..., ty+112; thread columns are 4tx..4tx+3 and
+// 32+4tx..32+4tx+3, so a warp's fragment reads hit distinct banks.
+__device__ __forceinline__ void compute_tile(const float* As, const float* Bs, int ty, int tx,
+                                             float (&acc)[8][8]) {
+#pragma unroll
+    for (int kq = 0; kq < BK; kq += 4) {
+        float4 a4[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            a4[r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD + kq);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b0 = *reinterpret_cast<const float4*>(Bs + (kq + kk) * BN + 4 * tx);
+            const float4 b1 = *reinterpret_cast<const float4*>(Bs + (kq + kk) * BN + 32 + 4 * tx);
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float a = kk == 0 ? a4[r].x : kk == 1 ? a4[r].y : kk == 2 ? a4[r].z : a4[r].w;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(a, b[j], acc[r][j]);
+            }
+        }
+    }
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p) {
+    extern __shared__ __align__(16) float smem[];
+    float* As = smem;                              // [STAGES][BM][A_LD]
+    float* Bs = smem + STAGES * A_STAGE_FLOATS;    // [STAGES][BK][BN]
+    const int tid = threadIdx.x;
+    const int ty = tid >> 3, tx = tid & 7;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int KT = (p.K + BK - 1) / BK;
+
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[r][j] = 0.0f;
+
+    if constexpr (STAGES == 1) {
+        for (int kt = 0; kt < KT; ++kt) {
+            load_tile(p, m0, n0, kt, As, Bs);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();  // read after write: every thread's copies landed
+            compute_tile(As, Bs, ty, tx, acc);
+            __syncthreads();  // write after read: nobody still reads the buffer
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s) {
+            if (s < KT) load_tile(p, m0, n0, s, As + s * A_STAGE_FLOATS, Bs + s * B_STAGE_FLOATS);
+            cp_async_commit();  // always commit: a fixed number of groups stays in flight
+        }
+        for (int kt = 0; kt < KT; ++kt) {
+            cp_async_wait<STAGES - 2>();  // this thread's copies of tile kt landed
+            __syncthreads();              // ... everyone's, and slot (kt-1) % S is free
+            const int nk = kt + STAGES - 1;
+            if (nk < KT) {
+                const int ns = nk % STAGES;
+                load_tile(p, m0, n0, nk, As + ns * A_STAGE_FLOATS, Bs + ns * B_STAGE_FLOATS);
+            }
+            cp_async_commit();
+            const int cs = kt % STAGES;
+            compute_tile(As + cs * A_STAGE_FLOATS, Bs + cs * B_STAGE_FLOATS, ty, tx, acc);
+        }
+        cp_async_wait<0>();
+    }
+
+    // Epilogue: C = alpha*acc + beta*C, masked at the M and N edges.
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int gm = m0 + ty + 16 * r;
+        if (gm >= p.M) continue;
+        float* crow = p.C + static_cast<long long>(gm) * p.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int gn = n0 + 32 * h + 4 * tx;
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = p.alpha * acc[r][4 * h + j];
+            if (gn + 4 <= p.N) {
+                float4* cp = reinterpret_cast<float4*>(crow + gn);
+                if (p.beta != 0.0f) {
+                    const float4 o = *cp;
+                    v[0] = fmaf(p.beta, o.x, v[0]);
+                    v[1] = fmaf(p.beta, o.y, v[1]);
+                    v[2] = fmaf(p.beta, o.z, v[2]);
+                    v[3] = fmaf(p.beta, o.w, v[3]);
+                }
+                *cp = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (gn + j < p.N) {
+                        float o = v[j];
+                        if (p.beta != 0.0f) o = fmaf(p.beta, crow[gn + j], o);
+                        crow[gn + j] = o;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int S>
+int launch_stages(const SimtParams& p, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(S) * (A_STAGE_FLOATS + B_STAGE_FLOATS) * sizeof(float);
+    if (smem > 48 * 1024) {
+        // A per-device attribute: set it once on each device used.
+        static std::mutex mu;
+        static bool done[64] = {false};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
+        std::lock_guard<std::mutex> g(mu);
+        if (!done[dev]) {
+            if (cudaFuncSetAttribute(sgemm_simt_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return GEMM_ERR_LAUNCH;
+            done[dev] = true;
+        }
+    }
+    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+    sgemm_simt_kernel<S><<<grid, THREADS, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+__global__ void scale_kernel(long long M, long long N, void* C, long long ldc, int out_bf16,
+                             float beta) {
+    const long long total = M * N;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long i = idx / N, j = idx - i * N;
+        if (out_bf16) {
+            __nv_bfloat16* c = static_cast<__nv_bfloat16*>(C) + i * ldc + j;
+            *c = beta == 0.0f ? __float2bfloat16_rn(0.0f) : __float2bfloat16_rn(beta * __bfloat162float(*c));
+        } else {
+            float* c = static_cast<float*>(C) + i * ldc + j;
+            *c = beta == 0.0f ? 0.0f : beta * *c;
+        }
+    }
+}
+
+}  // namespace
+
+int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
+    SimtParams p;
+    p.M = static_cast<int>(L.M);
+    p.N = static_cast<int>(L.N);
+    p.K = static_cast<int>(L.K);
+    p.A = L.A;
+    p.lda = L.lda;
+    p.B = L.B;
+    p.ldb = L.ldb;
+    p.C = L.C;
+    p.ldc = L.ldc;
+    p.alpha = L.alpha;
+    p.beta = L.beta;
+    if ((p.M + BM - 1) / BM > 65535) return GEMM_ERR_UNSUPPORTED;
+    switch (L.stages) {
+        case 1: return launch_stages<1>(p, stream);
+        case 2: return launch_stages<2>(p, stream);
+        case 3: return launch_stages<3>(p, stream);
+        case 4: return launch_stages<4>(p, stream);
+        default: return GEMM_ERR_ARG;
+    }
+}
+
+int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,
+                 cudaStream_t stream) {
+    const long long total = M * N;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    if (blocks < 1) blocks = 1;
+    scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, C, ldc, out_bf16, beta);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+}  // namespace ssp

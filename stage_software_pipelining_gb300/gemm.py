@@ -1,0 +1,185 @@
+"""ctypes binding over libgemm.so's C ABI (include/gemm.h).
+
+Argument marshalling only: tensors become (pointer, leading dimension) pairs
+and a dtype code; all arithmetic runs in the CUDA kernels of libgemm.so.
+If the library is missing the first call raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .workloads import GEMM_BF16_BF16, GEMM_BF16_F32, GEMM_F16_F32, GEMM_F32
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_ARG = -1
+GEMM_ERR_UNSUPPORTED = -2
+GEMM_ERR_ALIGN = -3
+GEMM_ERR_LAUNCH = -4
+GEMM_ERR_TIMEOUT = -5
+GEMM_ERR_CUDA = -6
+
+# Every extern "C" symbol include/gemm.h declares.
+EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
+           "gemm_status_string", "gemm_max_stages", "gemm_debug_set")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = "gemm"):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgemm.so and declare its signatures.  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path == LIB_PATH:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                "g.build()'); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        i64, p, i32, f32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        base = [i64, i64, i64, p, i64, p, i64, p, i64, f32, f32, i32, i32]
+        lib.gemm.argtypes = base + [p]
+        lib.gemm_ex.argtypes = base + [i32, i32, p]
+        lib.gemm_checked.argtypes = base + [i32, i32, p]
+        lib.gemm_host.argtypes = base + [i32, i32, p]
+        for name in ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
+                     "gemm_max_stages", "gemm_debug_set"):
+            getattr(lib, name).restype = i32
+        lib.gemm_host_release.argtypes = []
+        lib.gemm_status_string.argtypes = [i32]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_max_stages.argtypes = [i32, i32]
+        lib.gemm_debug_set.argtypes = [i64, i32]
+        if path == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().gemm_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def dtype_code(a_dtype: torch.dtype, c_dtype: torch.dtype) -> int:
+    table = {(torch.float32, torch.float32): GEMM_F32,
+             (torch.float16, torch.float32): GEMM_F16_F32,
+             (torch.bfloat16, torch.float32): GEMM_BF16_F32,
+             (torch.bfloat16, torch.bfloat16): GEMM_BF16_BF16}
+    try:
+        return table[(a_dtype, c_dtype)]
+    except KeyError:
+        raise ValueError(f"unsupported type pair {a_dtype} -> {c_dtype}") from None
+
+
+def _row_ld(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    r, c = t.shape
+    if r > 1 and c > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    return max(t.stride(0), c, 1) if r > 1 else max(c, 1)
+
+
+def _b_ld(B: torch.Tensor):
+    """(ldb, b_col_major) for B as a K x N matrix."""
+    if B.dim() != 2:
+        raise ValueError("B must be 2-D")
+    K, N = B.shape
+    if B.numel() == 0 or B.stride(1) == 1 and (K <= 1 or B.stride(0) >= N):
+        return (max(B.stride(0), N, 1) if K > 1 else max(N, 1)), 0
+    if B.stride(0) == 1:
+        return (max(B.stride(1), K, 1) if N > 1 else max(K, 1)), 1
+    raise ValueError("B must be row-major or column-major")
+
+
+def _args(A, B, C):
+    if A.dim() != 2 or B.dim() != 2 or C.dim() != 2:
+        raise ValueError("A, B and C must be 2-D")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, "
+                         f"C {tuple(C.shape)}")
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have the same dtype")
+    lda = _row_ld(A, "A")
+    ldb, bcm = _b_ld(B)
+    ldc = _row_ld(C, "C")
+    return M, N, K, lda, ldb, bcm, ldc, dtype_code(A.dtype, C.dtype)
+
+
+def default_stages(dtype: int) -> int:
+    return 2 if dtype == GEMM_F32 else 4
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+         beta: float = 0.0, stages: int | None = None, tile_n: int = 0,
+         stream: torch.cuda.Stream | None = None, checked: bool = False) -> torch.Tensor:
+    """C = alpha*A@B + beta*C in place on the GPU (libgemm.so gemm_ex / gemm_checked).
+
+    A: M x K row-major; B: K x N row-major, or column-major as a transposed
+    view of an N x K tensor; C: M x N row-major, fp32 (or bf16 for bf16 inputs).
+    Raises GemmError on a non-OK status.  Returns C.
+    """
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA tensor (use gemm_host for host buffers)")
+    M, N, K, lda, ldb, bcm, ldc, code = _args(A, B, C)
+    st = default_stages(code) if stages is None else int(stages)
+    s = (stream or torch.cuda.current_stream(C.device)).cuda_stream
+    lib = load_library()
+    fn = lib.gemm_checked if checked else lib.gemm_ex
+    with torch.cuda.device(C.device):
+        status = fn(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                    float(alpha), float(beta), code, st, bcm, int(tile_n), s)
+    if status != GEMM_OK:
+        raise GemmError(status, "gemm_checked" if checked else "gemm_ex")
+    return C
+
+
+def gemm_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
+              beta: float = 0.0, stages: int | None = None, tile_n: int = 0,
+              stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """The same operation on HOST tensors (libgemm.so gemm_host): copies in,
+    computes on the current device, copies C back, synchronises."""
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if t.device.type != "cpu":
+            raise ValueError(f"{n} must be a host tensor")
+    M, N, K, lda, ldb, bcm, ldc, code = _args(A, B, C)
+    st = default_stages(code) if stages is None else int(stages)
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    status = load_library().gemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                                      C.data_ptr(), ldc, float(alpha), float(beta), code, st,
+                                      bcm, int(tile_n), s)
+    if status != GEMM_OK:
+        raise GemmError(status, "gemm_host")
+    return C
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point with raw arguments (tests of the argument checks)."""
+    return int(getattr(load_library(), name)(*args))
+
+
+def max_stages(dtype: int, tile_n: int = 0) -> int:
+    return int(load_library().gemm_max_stages(int(dtype), int(tile_n)))
+
+
+def debug_set(wait_limit_ns: int = 0, withhold_arrive: int = -1) -> None:
+    load_library().gemm_debug_set(int(wait_limit_ns), int(withhold_arrive))

@@ -1,0 +1,171 @@
+"""The C-ABI library (no GPU needed): it builds, loads, exports every symbol
+include/gemm.h declares, and its host-side argument checks answer before any
+CUDA call is made.  No test here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from stage_software_pipelining_gb300 import build as gemm_build
+from stage_software_pipelining_gb300 import gemm as G
+from stage_software_pipelining_gb300.workloads import (GEMM_BF16_BF16, GEMM_BF16_F32,
+                                                       GEMM_F16_F32, GEMM_F32)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+# Fake device addresses: the checks below reject the call before any pointer
+# is used, so these are never dereferenced.
+P = 0x7F0000000000
+NULL = None
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gemm_build.build()
+    return G.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm\w*)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(G.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", G.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for name in declared_functions():
+        assert name in exported, name
+
+
+def gemm_ex(lib, M, N, K, A=P, lda=None, B=P, ldb=None, C=P, ldc=None, alpha=1.0, beta=0.0,
+            dtype=GEMM_BF16_F32, stages=4, bcm=0, tile_n=0):
+    lda = K if lda is None else lda
+    ldb = (K if bcm else N) if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return lib.gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, bcm, tile_n,
+                       None)
+
+
+def test_negative_sizes_rejected(lib):
+    assert gemm_ex(lib, -1, 8, 8) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, -1, 8) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, -1) == G.GEMM_ERR_ARG
+
+
+def test_bad_dtype_and_stages(lib):
+    assert gemm_ex(lib, 8, 8, 8, dtype=7) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, dtype=-1) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, stages=0) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, stages=7) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=5) == G.GEMM_ERR_ARG
+    # 256-wide tiles hold at most 4 stages in shared memory
+    assert gemm_ex(lib, 8, 512, 8, stages=5, tile_n=256) == G.GEMM_ERR_UNSUPPORTED
+    assert gemm_ex(lib, 8, 8, 8, tile_n=192) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile_n=128) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, bcm=2) == G.GEMM_ERR_ARG
+
+
+def test_leading_dimensions_too_small(lib):
+    assert gemm_ex(lib, 8, 16, 24, lda=16) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 16, 24, ldb=8) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 16, 24, ldb=16, bcm=1) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 16, 24, ldc=8) == G.GEMM_ERR_ARG
+
+
+def test_null_pointers(lib):
+    assert gemm_ex(lib, 8, 16, 24, A=NULL) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 16, 24, B=NULL) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 16, 24, C=NULL) == G.GEMM_ERR_ARG
+
+
+def test_alignment_rules(lib):
+    assert gemm_ex(lib, 8, 16, 24, A=P + 2) == G.GEMM_ERR_ALIGN
+    assert gemm_ex(lib, 8, 16, 24, B=P + 8) == G.GEMM_ERR_ALIGN
+    assert gemm_ex(lib, 8, 16, 24, C=P + 4) == G.GEMM_ERR_ALIGN
+    # 16-bit inputs: lda must be a multiple of 8 elements (16 bytes)
+    assert gemm_ex(lib, 8, 16, 20, lda=20) == G.GEMM_ERR_ALIGN
+    assert gemm_ex(lib, 8, 16, 24, lda=28) == G.GEMM_ERR_ALIGN
+    # fp32 output: ldc a multiple of 4
+    assert gemm_ex(lib, 8, 18, 24, ldc=18) == G.GEMM_ERR_ALIGN
+    # bf16 output: ldc a multiple of 8
+    assert gemm_ex(lib, 8, 20, 24, ldc=20, dtype=GEMM_BF16_BF16) == G.GEMM_ERR_ALIGN
+    # fp32 SIMT: lda a multiple of 4
+    assert gemm_ex(lib, 8, 16, 6, lda=6, dtype=GEMM_F32, stages=2) == G.GEMM_ERR_ALIGN
+
+
+def test_column_major_b_only_on_tensor_cores(lib):
+    assert gemm_ex(lib, 8, 16, 24, dtype=GEMM_F32, stages=2, bcm=1) == G.GEMM_ERR_UNSUPPORTED
+
+
+def test_oversized_dimensions(lib):
+    big = 2**31
+    assert gemm_ex(lib, big, 16, 16, lda=16) == G.GEMM_ERR_UNSUPPORTED
+
+
+def test_empty_output_is_a_noop(lib):
+    # M == 0 or N == 0 returns before touching CUDA, even with fake pointers
+    assert gemm_ex(lib, 0, 16, 24) == G.GEMM_OK
+    assert gemm_ex(lib, 8, 0, 24) == G.GEMM_OK
+    assert lib.gemm(0, 0, 0, NULL, 1, NULL, 1, NULL, 1, 1.0, 0.0, GEMM_F16_F32, 2, None) == 0
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = lib.gemm_status_string(code).decode()
+        assert s.startswith("GEMM_")
+    assert "unknown" in lib.gemm_status_string(42).decode()
+
+
+def test_max_stages(lib):
+    assert lib.gemm_max_stages(GEMM_F32, 0) == 4
+    assert lib.gemm_max_stages(GEMM_BF16_F32, 256) == 4
+    assert lib.gemm_max_stages(GEMM_BF16_F32, 128) == 6
+    assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 6
+    assert lib.gemm_max_stages(GEMM_F32, 128) == G.GEMM_ERR_ARG
+    assert lib.gemm_max_stages(9, 0) == G.GEMM_ERR_ARG
+
+
+def test_host_entry_validates_first(lib):
+    assert lib.gemm_host(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+                         None) == G.GEMM_ERR_ARG
+    assert lib.gemm_host(0, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+                         None) == G.GEMM_OK
+
+
+def test_python_binding_marshalling():
+    import torch
+    A = torch.zeros(8, 24, dtype=torch.bfloat16)
+    Bt = torch.zeros(16, 24, dtype=torch.bfloat16)
+    C = torch.zeros(8, 16)
+    assert G._args(A, Bt.t(), C)[5] == 1          # column-major B detected
+    assert G._args(A, Bt.t().contiguous(), C)[5] == 0
+    M, N, K, lda, ldb, bcm, ldc, code = G._args(A, Bt.t(), C)
+    assert (M, N, K, lda, ldb, ldc, code) == (8, 16, 24, 24, 24, 16, GEMM_BF16_F32)
+    with pytest.raises(ValueError):
+        G._args(A, torch.zeros(23, 16, dtype=torch.bfloat16), C)
+    with pytest.raises(ValueError):
+        G.dtype_code(torch.float16, torch.float16)
+    with pytest.raises(ValueError):
+        G.gemm(A, Bt.t(), C)                      # host tensors on the device entry
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        G.load_library(str(tmp_path / "libgemm.so"))
+
+
+def test_ctypes_signatures_cover_exports(lib):
+    for name in G.EXPORTS:
+        fn = getattr(lib, name)
+        assert fn.restype in (ctypes.c_int, ctypes.c_char_p), name

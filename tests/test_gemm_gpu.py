@@ -1,0 +1,285 @@
+"""GPU parity tests: libgemm.so (through its C ABI) against the fp64 oracle.
+
+Every case draws seeded inputs from the workload generators, runs the CUDA
+path, and compares element by element with the oracle on the same host
+values (tolerances in gpu_helpers).  Sizes span several tiles and a ragged
+tail; the full-size workloads are checked on sampled entries.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import GuardedC, check_against_oracle, to_device_padded
+from stage_software_pipelining_gb300 import build as gemm_build
+from stage_software_pipelining_gb300 import gemm as G
+from stage_software_pipelining_gb300.workloads import (BY_NAME, GEMM_BF16_BF16, GEMM_BF16_F32,
+                                                       GEMM_F16_F32, GEMM_F32, OUT_DTYPE,
+                                                       make_inputs)
+
+pytestmark = pytest.mark.gpu
+
+TC_DTYPES = [GEMM_F16_F32, GEMM_BF16_F32, GEMM_BF16_BF16]
+BASE_FOR = {GEMM_F32: "fp32_256", GEMM_F16_F32: "fp16_2048", GEMM_BF16_F32: "bf16_8192_beta1",
+            GEMM_BF16_BF16: "bf16_ragged_colB"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library(gpu):
+    gemm_build.build()
+    G.load_library()
+    G.debug_set(0, -1)
+    yield
+    G.debug_set(0, -1)
+
+
+def workload(dtype, M, N, K, **kw):
+    w = BY_NAME[BASE_FOR[dtype]].resized(M, N, K)
+    return dataclasses.replace(w, **kw) if kw else w
+
+
+def run_gpu(inp, stages, tile_n=0, alpha=None, beta=None, checked=True, guard=True):
+    """Run the CUDA path on padded device copies; return (host C as float64, guard)."""
+    w = inp.workload
+    alpha = w.alpha if alpha is None else alpha
+    beta = w.beta if beta is None else beta
+    A = to_device_padded(inp.A)
+    B = to_device_padded(inp.B, col_major=w.b_col_major)
+    out_dt = OUT_DTYPE[w.dtype]
+    init = inp.C0 if inp.C0 is not None else None
+    gC = GuardedC(w.M, w.N, out_dt, init=init.cuda() if init is not None else None)
+    if init is None:
+        gC.view.fill_(float("nan") if beta == 0.0 else 0.0)
+    G.gemm(A, B, gC.view, alpha, beta, stages=stages, tile_n=tile_n, checked=checked)
+    torch.cuda.synchronize()
+    if guard:
+        gC.check()
+    return gC.view.double().cpu().numpy(), gC
+
+
+def oracle_full(inp, alpha=None, beta=None):
+    w = inp.workload
+    alpha = w.alpha if alpha is None else alpha
+    beta = w.beta if beta is None else beta
+    return oracle.gemm(inp.A, inp.B, inp.C0 if beta != 0.0 else None, alpha, beta)
+
+
+# --------------------------------------------------------------------------- SIMT fp32
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_simt_fp32_256_matches_oracle(stages):
+    inp = make_inputs(BY_NAME["fp32_256"])
+    out, _ = run_gpu(inp, stages)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, GEMM_F32, what=f"simt stages={stages}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (7, 15, 17), (129, 65, 33), (300, 200, 129),
+                                   (128, 64, 16), (255, 127, 1)])
+@pytest.mark.parametrize("stages", [1, 2])
+def test_simt_ragged_shapes(shape, stages):
+    M, N, K = shape
+    inp = make_inputs(workload(GEMM_F32, M, N, K))
+    out, _ = run_gpu(inp, stages)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, GEMM_F32, what=f"simt {shape} s={stages}")
+
+
+def test_simt_alpha_beta():
+    w = workload(GEMM_F32, 200, 136, 72, alpha=-0.5, beta=2.0)
+    inp = make_inputs(w)
+    inp.C0 = torch.rand(200, 136, generator=torch.Generator().manual_seed(5)) * 2 - 1
+    out, _ = run_gpu(inp, 2)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, GEMM_F32, beta=2.0, C0=inp.C0, what="simt alpha/beta")
+
+
+def test_simt_stage_invariance_bitwise():
+    inp = make_inputs(workload(GEMM_F32, 333, 250, 190))
+    outs = [run_gpu(inp, s)[0] for s in (1, 2, 3, 4)]
+    for s, o in zip((2, 3, 4), outs[1:]):
+        assert np.array_equal(o, outs[0]), f"SIMT stages={s} differs from stages=1"
+
+
+# --------------------------------------------------------------------------- tensor cores
+@pytest.mark.parametrize("dtype", TC_DTYPES)
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("b_col_major", [False, True])
+def test_tc_ragged_matches_oracle(dtype, tile_n, b_col_major):
+    # several 128 x tile_n tiles with ragged M, N and K tails
+    w = workload(dtype, 300, 520, 200, b_col_major=b_col_major, beta=0.0)
+    inp = make_inputs(w)
+    out, _ = run_gpu(inp, 4, tile_n=tile_n)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, dtype, what=f"tc dt={dtype} bn={tile_n} "
+                                                      f"colB={b_col_major}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (7, 15, 17), (128, 256, 64), (129, 257, 65),
+                                   (255, 129, 1000), (64, 1000, 8), (513, 384, 320)])
+@pytest.mark.parametrize("b_col_major", [False, True])
+def test_tc_shape_fuzz(shape, b_col_major):
+    M, N, K = shape
+    for dtype in (GEMM_BF16_F32, GEMM_F16_F32):
+        inp = make_inputs(workload(dtype, M, N, K, b_col_major=b_col_major, beta=0.0))
+        out, _ = run_gpu(inp, 3)
+        ref, absb = oracle_full(inp)
+        check_against_oracle(out, ref, absb, dtype, what=f"tc fuzz {shape} dt={dtype}")
+
+
+@pytest.mark.parametrize("tile_n,stages_list", [(128, [1, 2, 3, 4, 5, 6]), (256, [1, 2, 3, 4])])
+@pytest.mark.parametrize("dtype", TC_DTYPES)
+def test_tc_stage_invariance_bitwise(tile_n, stages_list, dtype):
+    """The ring depth changes timing only: every stage count gives the same bits."""
+    w = workload(dtype, 384, 640, 520, beta=0.0)
+    inp = make_inputs(w)
+    outs = {s: run_gpu(inp, s, tile_n=tile_n)[0] for s in stages_list}
+    ref, absb = oracle_full(inp)
+    check_against_oracle(outs[stages_list[0]], ref, absb, dtype, what="tc invariance base")
+    for s in stages_list[1:]:
+        assert np.array_equal(outs[s], outs[stages_list[0]], equal_nan=True), \
+            f"stages={s} differs from stages={stages_list[0]} (tile_n={tile_n})"
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 1.0), (-0.5, 2.0), (2.0, -1.0), (0.25, 0.0)])
+@pytest.mark.parametrize("dtype", TC_DTYPES)
+def test_tc_alpha_beta(alpha, beta, dtype):
+    w = workload(dtype, 260, 300, 136, alpha=alpha, beta=beta)
+    inp = make_inputs(w)
+    if inp.C0 is None and beta != 0.0:
+        gen = torch.Generator().manual_seed(99)
+        inp.C0 = (torch.rand(260, 300, generator=gen) * 2 - 1).to(OUT_DTYPE[dtype])
+    out, _ = run_gpu(inp, 2, alpha=alpha, beta=beta)
+    ref, absb = oracle_full(inp, alpha, beta)
+    check_against_oracle(out, ref, absb, dtype, beta=beta, C0=inp.C0,
+                         what=f"alpha={alpha} beta={beta}")
+
+
+@pytest.mark.parametrize("dtype", [GEMM_F32] + TC_DTYPES)
+def test_beta_zero_does_not_read_c(dtype):
+    inp = make_inputs(workload(dtype, 140, 136, 40, beta=0.0))
+    out, _ = run_gpu(inp, 2)           # C is NaN-filled before the call
+    assert np.isfinite(out).all()
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, dtype, what="beta=0 NaN C")
+
+
+@pytest.mark.parametrize("dtype", [GEMM_F32, GEMM_BF16_F32, GEMM_BF16_BF16])
+def test_k_zero_and_alpha_zero_scale_c(dtype):
+    out_dt = OUT_DTYPE[dtype]
+    C0 = (torch.rand(70, 48, generator=torch.Generator().manual_seed(3)) * 2 - 1).to(out_dt)
+    A = torch.empty(70, 8, dtype=G_in(dtype), device="cuda")
+    B = torch.empty(8, 48, dtype=G_in(dtype), device="cuda")
+    for K in (0, 8):
+        C = C0.cuda()
+        Ak = A[:, :K] if K else torch.empty(70, 0, dtype=A.dtype, device="cuda")
+        Bk = B[:K] if K else torch.empty(0, 48, dtype=B.dtype, device="cuda")
+        if K:
+            Ak.fill_(float("inf"))          # alpha == 0 must not read A or B
+        G.gemm(Ak, Bk, C, 0.0 if K else 1.0, -0.5, stages=2, checked=True)
+        expect = (-0.5 * C0.double()).to(out_dt).double()
+        assert torch.equal(C.double().cpu(), expect)
+
+
+def G_in(dtype):
+    from stage_software_pipelining_gb300.workloads import IN_DTYPE
+    return IN_DTYPE[dtype]
+
+
+def test_empty_m_or_n_is_a_noop():
+    C = torch.full((0, 16), 1.0, device="cuda")
+    G.gemm(torch.zeros(0, 8, dtype=torch.bfloat16, device="cuda"),
+           torch.zeros(8, 16, dtype=torch.bfloat16, device="cuda"), C, checked=True)
+
+
+# --------------------------------------------------------------------------- fault path
+def test_withheld_arrive_times_out_and_context_survives():
+    """Block 0's producer skips one stage: the MMA wait must run out, the
+    kernel must return GEMM_ERR_TIMEOUT (no hang, no trap), and the next
+    GEMM on the same context must be correct."""
+    inp = make_inputs(workload(GEMM_BF16_F32, 256, 512, 512, beta=0.0))
+    A = to_device_padded(inp.A)
+    B = to_device_padded(inp.B)
+    C = torch.zeros(256, 512, device="cuda")
+    try:
+        G.debug_set(50_000_000, 3)      # 50 ms per wait; withhold K tile 3
+        with pytest.raises(G.GemmError) as e:
+            G.gemm(A, B, C, stages=2, checked=True)
+        assert e.value.status == G.GEMM_ERR_TIMEOUT
+    finally:
+        G.debug_set(0, -1)
+    G.gemm(A, B, C, stages=2, checked=True)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(C.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
+                         what="after timeout")
+
+
+# --------------------------------------------------------------------------- host entry
+@pytest.mark.parametrize("dtype", [GEMM_F32, GEMM_BF16_F32, GEMM_BF16_BF16])
+def test_host_entry_matches_device_entry(dtype):
+    w = workload(dtype, 190, 264, 96, beta=0.0, b_col_major=(dtype == GEMM_BF16_BF16))
+    inp = make_inputs(w)
+    out_dev, _ = run_gpu(inp, 2)
+    Ch = torch.zeros(190, 264, dtype=OUT_DTYPE[dtype]).pin_memory()
+    G.gemm_host(inp.A.pin_memory(), inp.B, Ch, stages=2)
+    assert np.array_equal(Ch.double().numpy(), out_dev)
+
+
+# --------------------------------------------------------------------------- full-size workloads
+def sample_indices(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    edge_r = [0, 1, 127, 128, M // 2, M - 2, M - 1]
+    edge_c = [0, 1, 15, 16, 255, 256, N // 2, N - 2, N - 1]
+    rows = [r for r in edge_r for _ in edge_c]
+    cols = [c for _ in edge_r for c in edge_c]
+    rows += list(rng.integers(0, M, count))
+    cols += list(rng.integers(0, N, count))
+    return np.array(rows), np.array(cols)
+
+
+@pytest.mark.parametrize("name,stages,tile_n", [
+    ("fp32_2048", 2, 0),
+    ("fp16_2048", 4, 0),
+    ("bf16_8192_beta1", 4, 256),
+    ("bf16_ragged_colB", 4, 256),
+])
+def test_full_size_workload_sampled(name, stages, tile_n):
+    w = BY_NAME[name]
+    inp = make_inputs(w)
+    A = inp.A.cuda()
+    B = inp.B.t().contiguous().t().cuda() if w.b_col_major else inp.B.cuda()
+    assert (B.stride(0) == 1) == w.b_col_major
+    C = inp.C0.cuda() if inp.C0 is not None else torch.full((w.M, w.N), float("nan"),
+                                                            dtype=OUT_DTYPE[w.dtype], device="cuda")
+    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile_n=tile_n, checked=True)
+    rows, cols = sample_indices(w.M, w.N, 3000, 7)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref, absb = oracle.gemm_entries(inp.A, inp.B, inp.C0, w.alpha, w.beta, rows=rows, cols=cols)
+    c0s = inp.C0[torch.from_numpy(rows), torch.from_numpy(cols)] if inp.C0 is not None else None
+    check_against_oracle(got, ref, absb, w.dtype, beta=w.beta, C0=c0s, what=name)
+    if w.dtype == GEMM_BF16_BF16:
+        # Frobenius criterion on the fp32-output launch of the same kernel
+        C32 = torch.empty(w.M, w.N, device="cuda")
+        G.gemm(A, B, C32, w.alpha, 0.0, stages=stages, tile_n=tile_n, checked=True)
+        got32 = C32[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+        check_against_oracle(got32.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
+                             what=name + " fp32 twin")
+
+
+def test_full_size_stage_sweep_is_bitwise_invariant():
+    """At the 8192^3 bf16 size, every stage count of the 128-wide tile and of
+    the 256-wide tile gives identical bits (the sweep the benchmark times)."""
+    w = BY_NAME["bf16_8192_beta1"]
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    C0 = inp.C0.cuda()
+    for tile_n, stages in ((128, (1, 2, 3, 4, 5, 6)), (256, (1, 2, 3, 4))):
+        base = None
+        for s in stages:
+            C = C0.clone()
+            G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile_n=tile_n, checked=True)
+            if base is None:
+                base = C
+            else:
+                assert torch.equal(C, base), f"tile_n={tile_n} stages={s}"
