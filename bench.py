@@ -1,0 +1,460 @@
+"""Benchmark of the software-pipelined GEMM (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--stages S] [--tile-n T]
+                    [--no-sweep] [--no-e2e] [--no-cpu]
+
+A step is one call of the GEMM over the workload's matrices (the whole hot
+path: tile loop, N-stage ring, tcgen05 MMAs, epilogue).  The default workload
+is C = A*B + C with M = N = K = 8192, bf16 inputs, fp32 accumulation and
+fp32 C (beta = 1): A, B and C (805 MB) are larger than the 129 MB L2, so no
+flush is needed between steps.  Inputs are seeded synthetic matrices.
+
+Reported: TFLOP/s (2*M*N*K per step) over exactly K timed steps measured with
+CUDA events on the launching stream; the dominant kernel's roofline (FLOPs
+per launch / mean launch time against the measured dense bf16 peak); the
+end-to-end number through the host-buffer entry point (host->device copies,
+GEMM, device->host copy per step); the stage sweep; SM clocks sampled during
+the timed region; and the CPU oracle timed on a bounded sample.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent
+replica of the same workload (the GEMM has no exchange step); value is the
+sum over ranks of the work divided by the slowest rank's time.
+
+--impl reference times the CPU oracle instead (fp64 triple loop on the host
+cores), each step a bounded block of C of the same workload, sized so that
+the whole run takes about two minutes; rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s & % of sm_103a MMA/FMA peak (bf16 8192³), vs pipeline stages"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "bf16_8192_beta1"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_bf16_8192_traffic.txt")
+KERNEL_SOURCES = ["stage_software_pipelining_gb300/csrc/gemm_tc_sm103a.cu",
+                  "stage_software_pipelining_gb300/csrc/ptx.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--stages", type=int, default=0, help="0 = the workload's default")
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str, stages: int, tile_n: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this launch configuration."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if (fields.get("kernel_sha") == kernel_hash() and fields.get("workload") == workload
+                and int(fields.get("stages", -1)) == stages
+                and int(fields.get("tile_n", -1)) == tile_n):
+            return float(fields["traffic_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (200 ms period)."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        loaded = [s for s in sm if smax and s >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    from stage_software_pipelining_gb300 import gemm as G
+    from stage_software_pipelining_gb300.workloads import BY_NAME, GEMM_F32, OUT_DTYPE, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.load_library()
+
+    w = BY_NAME[args.workload]
+    stages = args.stages or (2 if w.dtype == GEMM_F32 else 4)
+    tile_n = args.tile_n
+    if w.dtype != GEMM_F32 and tile_n == 0:
+        tile_n = 256 if stages <= 4 and w.N > 128 else 128
+    inp = make_inputs(w)
+    A = inp.A.to(dev)
+    B = (inp.B.t().contiguous().t() if w.b_col_major else inp.B).to(dev)
+    C = (inp.C0.to(dev) if inp.C0 is not None
+         else torch.zeros(w.M, w.N, dtype=OUT_DTYPE[w.dtype], device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(s=stages, t=tile_n):
+        G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile_n=t, stream=stream)
+
+    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream, checked=True)
+    for _ in range(args.warmup):
+        step()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    phys = int(visible[local]) if local < len(visible) and visible[local].isdigit() else local
+    sampler = ClockSampler(phys)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    barrier()
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    flops_step = w.flops
+    value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+
+    # the stage sweep (same workload, same launch stream)
+    sweep = []
+    if not args.no_sweep and w.dtype != GEMM_F32:
+        for tn, st_list in ((128, (1, 2, 3, 4, 5, 6)), (256, (1, 2, 3, 4))):
+            for s in st_list:
+                reps = max(10, min(200, args.steps // 10))
+                for _ in range(3):
+                    step(s, tn)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(dev)
+                e0.record(stream)
+                for _ in range(reps):
+                    step(s, tn)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms = e0.elapsed_time(e1) / reps
+                sweep.append({"tile_n": tn, "stages": s, "ms": round(ms, 4),
+                              "tflops": round(flops_step / (ms * 1e-3) / 1e12, 1)})
+    elif not args.no_sweep:
+        for s in (1, 2, 3, 4):
+            reps = max(10, min(200, args.steps // 10))
+            for _ in range(3):
+                step(s, 0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(reps):
+                step(s, 0)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            sweep.append({"stages": s, "ms": round(ms, 4),
+                          "tflops": round(flops_step / (ms * 1e-3) / 1e12, 1)})
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hA = inp.A.pin_memory()
+        hB = (inp.B.t().contiguous().pin_memory().t() if w.b_col_major
+              else inp.B.contiguous().pin_memory())
+        hC = (inp.C0.clone() if inp.C0 is not None else torch.zeros_like(C, device="cpu"))
+        hC = hC.pin_memory()
+        e2e_steps = max(3, min(30, args.steps))
+        G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream)
+        barrier()
+        h0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream)
+        barrier()
+        h_s = time.perf_counter() - h0
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([h_s], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            h_s = float(tt.item())
+        h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if w.beta != 0.0:
+            h2d += hC.numel() * hC.element_size()
+        d2h = hC.numel() * hC.element_size()
+        e2e = {"value": round(flops_step * e2e_steps * world / h_s / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": e2e_steps, "entry": "gemm_host (pinned host buffers)"}
+        G.load_library().gemm_host_release()
+
+    peaks, peak_kind = load_peaks()
+    if w.dtype == GEMM_F32:
+        roof = None
+    else:
+        sustained = elapsed_ms > 1000.0
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        achieved = flops_step / (launch_ms * 1e-3) / 1e12
+        traffic = committed_traffic(w.name, stages, tile_n)
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_kind": f"{peak_kind} cuBLAS bf16 8192^3, "
+                             f"{'sustained' if sustained else 'burst'}",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "algorithmic_flops_per_launch": flops_step,
+                "algorithmic_bytes_per_launch": algorithmic_bytes(w),
+                "kernel": "gemm_tc_kernel", "mean_launch_ms": round(launch_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(inp, budget_s=12.0)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC if w.name == DEFAULT_WORKLOAD else f"GEMM TFLOP/s ({w.name})",
+            "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w.dtype == GEMM_F32 else ("f16" if w.dtype == 1 else "bf16"),
+            "data": "synthetic (seeded)",
+            "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
+                       "alpha": w.alpha, "beta": w.beta, "stages": stages,
+                       "tile": "128x64x16 (SIMT)" if w.dtype == GEMM_F32
+                       else f"128x{tile_n}x64", "b_layout": "col" if w.b_col_major else "row",
+                       "l2": f"inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.0f} MB "
+                             f"touched per step > 129 MB); no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks, "stage_sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def describe(w):
+    from stage_software_pipelining_gb300.workloads import IN_DTYPE, OUT_DTYPE
+    i = str(IN_DTYPE[w.dtype]).replace("torch.", "")
+    o = str(OUT_DTYPE[w.dtype]).replace("torch.", "")
+    return (f"{w.name}: C = {w.alpha:g}*A*B + {w.beta:g}*C, M={w.M} N={w.N} K={w.K}, "
+            f"{i} inputs, fp32 accumulate, {o} output, B {'column' if w.b_col_major else 'row'}"
+            f"-major")
+
+
+def algorithmic_bytes(w) -> int:
+    from stage_software_pipelining_gb300.workloads import IN_DTYPE, OUT_DTYPE
+    import torch
+    si = torch.tensor([], dtype=IN_DTYPE[w.dtype]).element_size()
+    so = torch.tensor([], dtype=OUT_DTYPE[w.dtype]).element_size()
+    b = (w.M * w.K + w.K * w.N) * si + w.M * w.N * so
+    if w.beta != 0.0:
+        b += w.M * w.N * so
+    return int(b)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_block(inp, r0, r1, c0, c1, nthreads=0):
+    """Time the oracle on the block C[r0:r1, c0:c1] of the workload."""
+    import oracle
+    w = inp.workload
+    B = inp.B[:, c0:c1]
+    C0 = inp.C0[:, c0:c1] if (w.beta != 0.0 and inp.C0 is not None) else None
+    t = time.perf_counter()
+    oracle.gemm(inp.A, B, C0, w.alpha, w.beta, rows=(r0, r1), nthreads=nthreads,
+                with_abs=False)
+    return time.perf_counter() - t
+
+
+def _calibrate(inp, rows):
+    """Seconds per column of C for `rows` rows (one row per thread)."""
+    w = inp.workload
+    cols = min(w.N, 256)
+    return _oracle_block(inp, 0, rows, 0, cols) / cols
+
+
+def cpu_baseline(inp, budget_s: float):
+    """The oracle as it stands on the host cores, on a block sample of the workload."""
+    import oracle
+    w = inp.workload
+    cores = oracle.max_threads()
+    rows = max(1, min(w.M, cores))
+    per_col = _calibrate(inp, rows)          # seconds per column for `rows` rows
+    want_cols = budget_s / max(per_col, 1e-9)
+    if want_cols <= w.N:
+        cols = max(16, int(want_cols))
+    else:                                    # whole rows: grow the row count instead
+        cols = w.N
+        rows = max(rows, min(w.M, rows * int(want_cols / w.N)))
+    dt = _oracle_block(inp, 0, rows, 0, cols)
+    flops = 2.0 * rows * cols * w.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"C[0:{rows}, 0:{cols}] of the {w.name} workload (K={w.K}) = "
+                      f"{flops:.3e} FLOP, fp64 i-k-j loop, one row per OpenMP thread"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from stage_software_pipelining_gb300.workloads import BY_NAME, make_inputs
+    w = BY_NAME[args.workload]
+    inp = make_inputs(w)
+    cores = oracle.max_threads()
+    rows = max(1, min(w.M, cores))
+    # size each step so that warmup + steps take about two minutes of CPU time
+    per_col = _calibrate(inp, rows)
+    total_steps = max(args.steps + args.warmup, 1)
+    cols = max(16, min(w.N, int(120.0 / total_steps / max(per_col, 1e-9))))
+    n_blocks = max(1, (w.M // rows) * (w.N // cols))
+
+    def block(i):
+        b = i % n_blocks
+        r0 = (b % max(w.M // rows, 1)) * rows
+        c0 = (b // max(w.M // rows, 1)) * cols
+        return r0, min(r0 + rows, w.M), c0, min(c0 + cols, w.N)
+
+    for i in range(args.warmup):
+        _oracle_block(inp, *block(i))
+    t = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_block(inp, *block(args.warmup + i))
+    el = time.perf_counter() - t
+    flops = 2.0 * rows * cols * w.K * args.steps
+    value = flops / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC if w.name == DEFAULT_WORKLOAD
+        else f"GEMM TFLOP/s ({w.name})",
+        "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
+                   "sample_block_per_step": [rows, cols], "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"a {rows}x{cols} block of C per step (K={w.K}), "
+                                   f"fp64 i-k-j loop, one row per OpenMP thread"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -37,8 +37,17 @@ struct Checked {
     int tile_n;
 };
 
-Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-                 int64_t ldb, void* C, int64_t ldc, int dtype, int stages, int b_col_major,
+// With a single row in memory an operand's leading dimension is never used;
+// it is normalised to the row length rounded up to 16 bytes so that the
+// alignment rule (and the tensor map's stride rule) holds.
+int64_t single_row_ld(int64_t ld, int64_t cols, int size) {
+    const int64_t m = 16 / size;
+    const int64_t c = ld > cols ? ld : cols;
+    return (c + m - 1) / m * m;
+}
+
+Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, const void* B,
+                 int64_t& ldb, void* C, int64_t& ldc, int dtype, int stages, int b_col_major,
                  int tile_n) {
     Checked r{GEMM_OK, 0};
     if (dtype < GEMM_F32 || dtype > GEMM_BF16_BF16) return {GEMM_ERR_ARG, 0};
@@ -63,6 +72,9 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     if (!is_tc(dtype) && b_col_major) return {GEMM_ERR_UNSUPPORTED, 0};
     if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return {GEMM_ERR_UNSUPPORTED, 0};
     const int si = in_size(dtype), so = out_size(dtype);
+    if (M <= 1) lda = single_row_ld(lda, K, si);
+    if ((b_col_major ? N : K) <= 1) ldb = single_row_ld(ldb, b_col_major ? K : N, si);
+    if (M <= 1) ldc = single_row_ld(ldc, N, so);
     if (use_a && (!aligned16(A) || (lda * si) % 16 != 0)) return {GEMM_ERR_ALIGN, 0};
     if (use_b && (!aligned16(B) || (ldb * si) % 16 != 0)) return {GEMM_ERR_ALIGN, 0};
     if (use_c && (!aligned16(C) || (ldc * so) % 16 != 0)) return {GEMM_ERR_ALIGN, 0};
