@@ -58,7 +58,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--stages", type=int, default=0, help="0 = the workload's default")
-    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--tile", type=int, default=0,
+                    help="tensor-core tile code: 0 auto, 128 (128x128), 256 (128x256), "
+                         "512 (256x256 on a CTA pair)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -90,7 +92,12 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str, stages: int, tile_n: int):
+TILE_NAMES = {128: "128x128x64 (1 SM)", 256: "128x256x64 (1 SM)",
+              512: "256x256x64 (CTA pair, cta_group::2)"}
+TILE_MAX_STAGES = {128: 6, 256: 4, 512: 6}
+
+
+def committed_traffic(workload: str, stages: int, tile: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source for this launch configuration."""
     try:
@@ -102,7 +109,7 @@ def committed_traffic(workload: str, stages: int, tile_n: int):
                     fields[k.strip()] = v.strip()
         if (fields.get("kernel_sha") == kernel_hash() and fields.get("workload") == workload
                 and int(fields.get("stages", -1)) == stages
-                and int(fields.get("tile_n", -1)) == tile_n):
+                and int(fields.get("tile", -1)) == tile):
             return float(fields["traffic_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -175,10 +182,14 @@ def run_ours(args):
     G.load_library()
 
     w = BY_NAME[args.workload]
-    stages = args.stages or (2 if w.dtype == GEMM_F32 else 4)
-    tile_n = args.tile_n
-    if w.dtype != GEMM_F32 and tile_n == 0:
-        tile_n = 256 if stages <= 4 and w.N > 128 else 128
+    tile = args.tile
+    if w.dtype != GEMM_F32 and tile == 0:
+        tile = G.TILE_256x256_2SM if (w.M > 128 and w.N > 128) else \
+            (G.TILE_128x128 if w.N <= 128 else G.TILE_128x256)
+    if w.dtype == GEMM_F32:
+        stages = args.stages or 2
+    else:
+        stages = args.stages or TILE_MAX_STAGES[tile]
     inp = make_inputs(w)
     A = inp.A.to(dev)
     B = (inp.B.t().contiguous().t() if w.b_col_major else inp.B).to(dev)
@@ -186,10 +197,10 @@ def run_ours(args):
          else torch.zeros(w.M, w.N, dtype=OUT_DTYPE[w.dtype], device=dev))
     stream = torch.cuda.current_stream(dev)
 
-    def step(s=stages, t=tile_n):
-        G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile_n=t, stream=stream)
+    def step(s=stages, t=tile):
+        G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile=t, stream=stream)
 
-    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream, checked=True)
+    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile=tile, stream=stream, checked=True)
     for _ in range(args.warmup):
         step()
 
@@ -229,8 +240,8 @@ def run_ours(args):
     # the stage sweep (same workload, same launch stream)
     sweep = []
     if not args.no_sweep and w.dtype != GEMM_F32:
-        for tn, st_list in ((128, (1, 2, 3, 4, 5, 6)), (256, (1, 2, 3, 4))):
-            for s in st_list:
+        for tn in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM):
+            for s in range(1, TILE_MAX_STAGES[tn] + 1):
                 reps = max(10, min(200, args.steps // 10))
                 for _ in range(3):
                     step(s, tn)
@@ -243,7 +254,7 @@ def run_ours(args):
                 e1.record(stream)
                 torch.cuda.synchronize(dev)
                 ms = e0.elapsed_time(e1) / reps
-                sweep.append({"tile_n": tn, "stages": s, "ms": round(ms, 4),
+                sweep.append({"tile": TILE_NAMES[tn], "stages": s, "ms": round(ms, 4),
                               "tflops": round(flops_step / (ms * 1e-3) / 1e12, 1)})
     elif not args.no_sweep:
         for s in (1, 2, 3, 4):
@@ -271,11 +282,11 @@ def run_ours(args):
         hC = (inp.C0.clone() if inp.C0 is not None else torch.zeros_like(C, device="cpu"))
         hC = hC.pin_memory()
         e2e_steps = max(3, min(30, args.steps))
-        G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream)
+        G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile=tile, stream=stream)
         barrier()
         h0 = time.perf_counter()
         for _ in range(e2e_steps):
-            G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile_n=tile_n, stream=stream)
+            G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile=tile, stream=stream)
         barrier()
         h_s = time.perf_counter() - h0
         if world > 1:
@@ -299,7 +310,7 @@ def run_ours(args):
         sustained = elapsed_ms > 1000.0
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         achieved = flops_step / (launch_ms * 1e-3) / 1e12
-        traffic = committed_traffic(w.name, stages, tile_n)
+        traffic = committed_traffic(w.name, stages, tile)
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} cuBLAS bf16 8192^3, "
@@ -324,7 +335,7 @@ def run_ours(args):
             "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
                        "alpha": w.alpha, "beta": w.beta, "stages": stages,
                        "tile": "128x64x16 (SIMT)" if w.dtype == GEMM_F32
-                       else f"128x{tile_n}x64", "b_layout": "col" if w.b_col_major else "row",
+                       else TILE_NAMES[tile], "b_layout": "col" if w.b_col_major else "row",
                        "l2": f"inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.0f} MB "
                              f"touched per step > 129 MB); no flush",
                        "parallelism": f"replicas x{world}"},

@@ -73,6 +73,17 @@ typedef enum {
     GEMM_BF16_BF16 = 3
 } gemm_dtype_t;
 
+/* Tensor-core tile (gemm_ex's `tile`).  The 2-SM tile runs on a cluster of
+ * two CTAs with tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and
+ * 128 columns of B per K step and holds 128 rows of the 256 x 256 result. */
+typedef enum {
+    GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128,
+                                    else 128x128 (N <= 128) or 128x256 */
+    GEMM_TILE_128x128 = 128,     /* one CTA, stages 1..6 (32 KB per stage) */
+    GEMM_TILE_128x256 = 256,     /* one CTA, stages 1..4 (48 KB per stage) */
+    GEMM_TILE_256x256_2SM = 512  /* a CTA pair, stages 1..6 (32 KB per stage per CTA) */
+} gemm_tile_t;
+
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_ARG = -1,          /* bad size, leading dimension, pointer, dtype or stages */
@@ -94,7 +105,7 @@ typedef enum {
  *   stages     depth of the shared-memory ring: 1..6 on the tensor-core path,
  *              1..4 on the SIMT path
  *   stream     cudaStream_t
- * The tensor-core tile is 128 x 256 for stages <= 4 and 128 x 128 above.
+ * The tensor-core tile is GEMM_TILE_AUTO's choice.
  */
 int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
          void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, void* stream);
@@ -104,13 +115,13 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void
  *   b_col_major  0: B row-major (as gemm); 1: B column-major (element (k,j)
  *                at B[j*ldb + k], ldb >= K).  Column-major B is implemented on
  *                the tensor-core path only (GEMM_ERR_UNSUPPORTED for GEMM_F32).
- *   tile_n       tensor-core tile width: 0 = the gemm default, 128 or 256.
- *                128 allows stages 1..6, 256 allows stages 1..4 (shared-memory
- *                capacity).  Must be 0 on the SIMT path (its tile is 128 x 64).
+ *   tile         a gemm_tile_t (tensor-core path); a stage count above the
+ *                tile's limit gives GEMM_ERR_UNSUPPORTED.  Must be 0 on the
+ *                SIMT path (its tile is 128 x 64).
  */
 int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
             int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
-            int b_col_major, int tile_n, void* stream);
+            int b_col_major, int tile, void* stream);
 
 /*
  * gemm_checked -- gemm_ex, then synchronise `stream` and read (and clear) the
@@ -120,7 +131,7 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
  */
 int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                  int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype,
-                 int stages, int b_col_major, int tile_n, void* stream);
+                 int stages, int b_col_major, int tile, void* stream);
 
 /*
  * gemm_host -- the same operation on HOST buffers: copies A, B (and C when
@@ -131,7 +142,7 @@ int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
  */
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
-              int b_col_major, int tile_n, void* stream);
+              int b_col_major, int tile, void* stream);
 
 /* Frees gemm_host's cached device buffers on the current device. */
 int gemm_host_release(void);
@@ -139,9 +150,19 @@ int gemm_host_release(void);
 /* Human-readable name of a gemm_status_t (static storage). */
 const char* gemm_status_string(int status);
 
-/* Largest `stages` value accepted for a dtype and tile_n (as in gemm_ex), or
+/* Largest `stages` value accepted for a dtype and tile (as in gemm_ex), or
  * GEMM_ERR_ARG for an unknown combination. */
-int gemm_max_stages(int dtype, int tile_n);
+int gemm_max_stages(int dtype, int tile);
+
+/*
+ * gemm_plan -- the launch gemm_ex would make for these sizes, without making
+ * it: CTAs in the grid, CTAs per cluster (2 for the pair tile) and dynamic
+ * shared memory per CTA.  Needs a current CUDA device (it asks the runtime
+ * how many CTA pairs can be resident).  M == 0, N == 0 or K == 0 plans no
+ * GEMM kernel (grid 0).  Returns a gemm_status_t; outputs may be NULL.
+ */
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_major, int tile,
+              int* grid, int* cluster, int* smem_bytes);
 
 /*
  * gemm_debug_set -- test hook for the bounded waits (not thread-safe; affects

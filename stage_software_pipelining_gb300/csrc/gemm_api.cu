@@ -22,19 +22,30 @@ bool is_tc(int dtype) {
 int in_size(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
 int out_size(int dtype) { return dtype == GEMM_BF16_BF16 ? 2 : 4; }
 
-// Tensor-core tile width for a request (0 = invalid).
-int resolve_tile_n(int64_t N, int stages, int tile_n) {
-    if (tile_n == 128 || tile_n == 256) return tile_n;
-    if (tile_n != 0) return 0;
-    if (stages > ssp::kTcMaxStages256 || N <= 128) return 128;
-    return 256;
+// Tensor-core tile for a request (0 = invalid tile code).  The default is the
+// 256 x 256 tile on a CTA pair unless M or N is a single 128-wide tile.
+int resolve_tile(int64_t M, int64_t N, int tile) {
+    if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM)
+        return tile;
+    if (tile != GEMM_TILE_AUTO) return 0;
+    if (M > 128 && N > 128) return GEMM_TILE_256x256_2SM;
+    return N <= 128 ? GEMM_TILE_128x128 : GEMM_TILE_128x256;
+}
+
+int tile_max_stages(int tile) {
+    switch (tile) {
+        case GEMM_TILE_128x128: return ssp::kTcMaxStages128;
+        case GEMM_TILE_128x256: return ssp::kTcMaxStages256;
+        case GEMM_TILE_256x256_2SM: return ssp::kTcMaxStagesPair;
+        default: return 0;
+    }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Checked {
     int status;
-    int tile_n;
+    int tile;  // resolved gemm_tile_t (tensor-core path)
 };
 
 // With a single row in memory an operand's leading dimension is never used;
@@ -48,19 +59,18 @@ int64_t single_row_ld(int64_t ld, int64_t cols, int size) {
 
 Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, const void* B,
                  int64_t& ldb, void* C, int64_t& ldc, int dtype, int stages, int b_col_major,
-                 int tile_n) {
+                 int tile) {
     Checked r{GEMM_OK, 0};
     if (dtype < GEMM_F32 || dtype > GEMM_BF16_BF16) return {GEMM_ERR_ARG, 0};
     if (M < 0 || N < 0 || K < 0) return {GEMM_ERR_ARG, 0};
     if (b_col_major != 0 && b_col_major != 1) return {GEMM_ERR_ARG, 0};
     if (is_tc(dtype)) {
-        r.tile_n = resolve_tile_n(N, stages, tile_n);
-        if (r.tile_n == 0) return {GEMM_ERR_ARG, 0};
-        const int max_s = r.tile_n == 256 ? ssp::kTcMaxStages256 : ssp::kTcMaxStages128;
+        r.tile = resolve_tile(M, N, tile);
+        if (r.tile == 0) return {GEMM_ERR_ARG, 0};
         if (stages < 1 || stages > ssp::kTcMaxStages128) return {GEMM_ERR_ARG, 0};
-        if (stages > max_s) return {GEMM_ERR_UNSUPPORTED, 0};
+        if (stages > tile_max_stages(r.tile)) return {GEMM_ERR_UNSUPPORTED, 0};
     } else {
-        if (tile_n != 0) return {GEMM_ERR_ARG, 0};
+        if (tile != 0) return {GEMM_ERR_ARG, 0};
         if (stages < 1 || stages > ssp::kSimtMaxStages) return {GEMM_ERR_ARG, 0};
     }
     const bool use_a = M > 0 && K > 0;
@@ -81,20 +91,9 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, c
     return r;
 }
 
-int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-        void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, int b_col_major,
-        int tile_n, cudaStream_t stream) {
-    Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile_n);
-    if (v.status != GEMM_OK) return v.status;
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (K == 0 || alpha == 0.0f)
-        return ssp::scale_launch(M, N, C, ldc, dtype == GEMM_BF16_BF16, beta, stream);
-    if (dtype == GEMM_F32) {
-        ssp::SimtLaunch L{M, N, K, static_cast<const float*>(A), lda,
-                          static_cast<const float*>(B), ldb, static_cast<float*>(C), ldc,
-                          alpha, beta, stages};
-        return ssp::simt_launch(L, stream);
-    }
+ssp::TcLaunch tc_request(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
+                         int dtype, int stages, int b_col_major, int tile) {
     ssp::TcLaunch L;
     L.M = M;
     L.N = N;
@@ -111,9 +110,29 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     L.out_bf16 = dtype == GEMM_BF16_BF16;
     L.b_col_major = b_col_major;
     L.stages = stages;
-    L.tile_n = v.tile_n;
+    L.tile_n = tile == GEMM_TILE_128x128 ? 128 : 256;
+    L.pair = tile == GEMM_TILE_256x256_2SM;
     L.wait_limit_ns = g_wait_limit_ns;
     L.withhold_arrive = g_withhold_arrive;
+    return L;
+}
+
+int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+        void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, int b_col_major,
+        int tile, cudaStream_t stream) {
+    Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile);
+    if (v.status != GEMM_OK) return v.status;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (K == 0 || alpha == 0.0f)
+        return ssp::scale_launch(M, N, C, ldc, dtype == GEMM_BF16_BF16, beta, stream);
+    if (dtype == GEMM_F32) {
+        ssp::SimtLaunch L{M, N, K, static_cast<const float*>(A), lda,
+                          static_cast<const float*>(B), ldb, static_cast<float*>(C), ldc,
+                          alpha, beta, stages};
+        return ssp::simt_launch(L, stream);
+    }
+    const ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
+                                       stages, b_col_major, v.tile);
     return ssp::tc_launch(L, stream);
 }
 
@@ -150,16 +169,16 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void
 
 int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
             int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
-            int b_col_major, int tile_n, void* stream) {
-    return run(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, b_col_major, tile_n,
+            int b_col_major, int tile, void* stream) {
+    return run(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, b_col_major, tile,
                static_cast<cudaStream_t>(stream));
 }
 
 int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                  int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype,
-                 int stages, int b_col_major, int tile_n, void* stream) {
+                 int stages, int b_col_major, int tile, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int st = run(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, b_col_major, tile_n,
+    int st = run(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, b_col_major, tile,
                  s);
     if (st != GEMM_OK) return st;
     if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -171,8 +190,8 @@ int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
-              int b_col_major, int tile_n, void* stream) {
-    Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile_n);
+              int b_col_major, int tile, void* stream) {
+    Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile);
     if (v.status != GEMM_OK) return v.status;
     if (M == 0 || N == 0) return GEMM_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -199,7 +218,7 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     if (beta != 0.0f && cudaMemcpyAsync(dC, C, c_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return GEMM_ERR_CUDA;
     st = run(M, N, K, need_ab ? dA : A, lda, need_ab ? dB : B, ldb, dC, ldc, alpha, beta, dtype,
-             stages, b_col_major, tile_n, s);
+             stages, b_col_major, tile, s);
     if (st != GEMM_OK) return st;
     if (cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -233,12 +252,42 @@ const char* gemm_status_string(int status) {
     }
 }
 
-int gemm_max_stages(int dtype, int tile_n) {
-    if (dtype == GEMM_F32) return tile_n == 0 ? ssp::kSimtMaxStages : GEMM_ERR_ARG;
+int gemm_max_stages(int dtype, int tile) {
+    if (dtype == GEMM_F32) return tile == 0 ? ssp::kSimtMaxStages : GEMM_ERR_ARG;
     if (!is_tc(dtype)) return GEMM_ERR_ARG;
-    if (tile_n == 256) return ssp::kTcMaxStages256;
-    if (tile_n == 128 || tile_n == 0) return ssp::kTcMaxStages128;
-    return GEMM_ERR_ARG;
+    if (tile == GEMM_TILE_AUTO) return ssp::kTcMaxStages128;
+    const int m = tile_max_stages(tile);
+    return m > 0 ? m : GEMM_ERR_ARG;
+}
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_major, int tile,
+              int* grid, int* cluster, int* smem_bytes) {
+    // Validation with placeholder (aligned, non-null) pointers: only the
+    // sizes, types, stages and tile are being planned.
+    const void* P = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    const int si = in_size(dtype >= GEMM_F32 && dtype <= GEMM_BF16_BF16 ? dtype : 0);
+    const int so = out_size(dtype);
+    auto pad = [](int64_t x, int64_t size) { return (x + 16 / size - 1) / (16 / size) * (16 / size); };
+    int64_t lda = pad(K > 0 ? K : 1, si), ldb = pad(b_col_major ? K : N, si), ldc = pad(N > 0 ? N : 1, so);
+    if (ldb < 1) ldb = 16 / si;
+    Checked v = validate(M, N, K, P, lda, P, ldb, const_cast<void*>(P), ldc, dtype, stages,
+                         b_col_major, tile);
+    if (v.status != GEMM_OK) return v.status;
+    if (M == 0 || N == 0 || K == 0) {
+        if (grid) *grid = 0;
+        if (cluster) *cluster = 1;
+        if (smem_bytes) *smem_bytes = 0;
+        return GEMM_OK;
+    }
+    if (dtype == GEMM_F32) {
+        if (grid) *grid = static_cast<int>(((M + 127) / 128) * ((N + 63) / 64));
+        if (cluster) *cluster = 1;
+        if (smem_bytes) *smem_bytes = stages * (128 * 20 + 16 * 64) * 4;
+        return GEMM_OK;
+    }
+    const ssp::TcLaunch L = tc_request(M, N, K, P, lda, P, ldb, const_cast<void*>(P), ldc, 1.0f,
+                                       0.0f, dtype, stages, b_col_major, v.tile);
+    return ssp::tc_plan(L, grid, cluster, smem_bytes);
 }
 
 int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive) {

@@ -66,7 +66,7 @@ struct TcParams {
     int tiles_m, tiles_n, num_tiles, k_tiles;
     int group_m;
     int stages;
-    int bn;
+    int bn;           // tile width (columns of C per tile)
     int b_mn_major;
     int out_bf16;
     uint32_t idesc;
@@ -78,7 +78,8 @@ struct TcParams {
 };
 
 struct SharedCtl {
-    unsigned long long bar[2 * kTcMaxStages128 + 5];  // full[S], empty[S], tfull[2], tempty[2], drain
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    unsigned long long bar[2 * kTcMaxStages128 + 5];
     uint32_t tmem_base;
     int abort;
 };
@@ -101,10 +102,21 @@ __device__ __forceinline__ void record_timeout(int role, int iter) {
     }
 }
 
+// Raise the abort flag of this CTA and, for a CTA pair, of the peer CTA.
+template <bool PAIR>
+__device__ __forceinline__ void raise_abort(volatile int* abort, uint32_t peer_rank) {
+    *abort = 1;
+    if constexpr (PAIR) {
+        st_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(abort)), peer_rank), 1u);
+    }
+}
+
 // Wait for the phase of `bar` with parity `parity`; give up after
 // limit_ns or when another role has raised the abort flag.
+template <bool PAIR>
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                             unsigned long long limit_ns, int role, int iter) {
+                                             unsigned long long limit_ns, int role, int iter,
+                                             uint32_t peer_rank) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
@@ -113,7 +125,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 record_timeout(role, iter);
-                *abort = 1;
+                raise_abort<PAIR>(abort, peer_rank);
                 return false;
             }
         }
@@ -207,6 +219,17 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, int row, int 
     }
 }
 
+// PAIR = false: one CTA computes a 128 x bn tile with tcgen05.mma.cta_group::1.
+// PAIR = true: a cluster of two CTAs computes a 256 x bn tile with
+// tcgen05.mma.cta_group::2: CTA rank r stages rows 128r..128r+127 of the A
+// tile and columns (bn/2)r..(bn/2)r+bn/2-1 of the B tile, the leader (rank 0)
+// issues every MMA, and each CTA's TMEM receives its own 128 rows of C.
+// Both CTAs' copies of a stage complete on the LEADER's full[s], which the
+// leader arms with the pair's byte count; the MMA's commit frees the slot in
+// both CTAs (multicast), and both epilogues release the accumulator to the
+// leader.  (Relaying the peer's stage through a thread instead costs one
+// remote round trip per stage and capped the pair at ~60 % of the MMA rate.)
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
@@ -214,14 +237,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Swizzled TMA destinations and UMMA operands want 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int TILE_M = PAIR ? 2 * BM : BM;
     const int S = p.stages;
-    const int b_stage_bytes = p.bn * BK * 2;
+    const int b_cols = PAIR ? p.bn / 2 : p.bn;   // B columns staged by this CTA
+    const int b_stage_bytes = b_cols * BK * 2;
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * A_STAGE_BYTES;
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(b_ring + S * b_stage_bytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? (cluster_ctarank() & 1u) : 0u;
+    const uint32_t peer_rank = rank ^ 1u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int num_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+
     const uint32_t bar0 = smem_addr(&ctl->bar[0]);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -230,6 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
     volatile int* abort_flag = &ctl->abort;
     const uint32_t tmem_cols = 2u * p.bn;  // two accumulators: 256 or 512 columns
+    constexpr uint16_t kPairMask = 0x3;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -238,18 +270,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4 * 32);
+            mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrive per epilogue warp (both CTAs)
         }
         mbar_init(drain_bar, 1);
         ctl->abort = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&ctl->tmem_base), tmem_cols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_addr(&ctl->tmem_base), tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(&ctl->tmem_base), tmem_cols);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
@@ -259,30 +297,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
             const uint32_t stage_bytes = A_STAGE_BYTES + b_stage_bytes;
+            // The leader's full[s] counts the bytes of both CTAs of a pair.
+            const uint32_t armed_bytes = PAIR ? 2u * stage_bytes : stage_bytes;
+            const uint32_t leader_full0 = PAIR ? mapa_shared(full_bar(0), 0u) : full_bar(0);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = unit; ok && t < p.num_tiles; t += num_units) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
+                const int a_row = tm * TILE_M + static_cast<int>(rank) * BM;
+                const int b_col = tn * p.bn + static_cast<int>(rank) * b_cols;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
-                    if (!bounded_wait(empty_bar(s), ph ^ 1u, abort_flag, p.wait_limit_ns,
-                                      ROLE_PRODUCER, it)) {
+                    if (!bounded_wait<PAIR>(empty_bar(s), ph ^ 1u, abort_flag, p.wait_limit_ns,
+                                            ROLE_PRODUCER, it, peer_rank)) {
                         ok = false;
                         break;
                     }
                     if (!(it == p.withhold && blockIdx.x == 0)) {
                         const uint32_t a_dst = smem_addr(a_ring + s * A_STAGE_BYTES);
                         const uint32_t b_dst = smem_addr(b_ring + s * b_stage_bytes);
-                        mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-                        tma_load_2d(a_dst, &tmA, full_bar(s), kt * BK, tm * BM);
-                        if (p.b_mn_major) {
-                            for (int j = 0; j < p.bn / 64; ++j)
-                                tma_load_2d(b_dst + j * B_BOX_BYTES, &tmB, full_bar(s),
-                                            tn * p.bn + 64 * j, kt * BK);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), armed_bytes);
+                        if (PAIR && !leader) {
+                            const uint32_t bar = leader_full0 + 8u * s;
+                            tma_load_2d_pair(a_dst, &tmA, bar, kt * BK, a_row);
+                            if (p.b_mn_major) {
+                                for (int j = 0; j < b_cols / 64; ++j)
+                                    tma_load_2d_pair(b_dst + j * B_BOX_BYTES, &tmB, bar,
+                                                     b_col + 64 * j, kt * BK);
+                            } else {
+                                tma_load_2d_pair(b_dst, &tmB, bar, kt * BK, b_col);
+                            }
                         } else {
-                            tma_load_2d(b_dst, &tmB, full_bar(s), kt * BK, tn * p.bn);
+                            tma_load_2d(a_dst, &tmA, full_bar(s), kt * BK, a_row);
+                            if (p.b_mn_major) {
+                                for (int j = 0; j < b_cols / 64; ++j)
+                                    tma_load_2d(b_dst + j * B_BOX_BYTES, &tmB, full_bar(s),
+                                                b_col + 64 * j, kt * BK);
+                            } else {
+                                tma_load_2d(b_dst, &tmB, full_bar(s), kt * BK, b_col);
+                            }
                         }
                     }
                     ++it;
@@ -293,18 +348,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) {
-                // Let every copy this thread issued land before the CTA exits.
-                const int first = it - S > 0 ? it - S : 0;
-                for (int j = first; j < it; ++j) {
-                    if (j == p.withhold && blockIdx.x == 0) continue;
-                    drain_wait(full_bar(j % S), static_cast<uint32_t>((j / S) & 1), p.wait_limit_ns);
+                if (leader) {
+                    // Let every copy this CTA armed land before the CTA exits (for
+                    // a pair this also covers the peer's copies of those stages).
+                    const int first = it - S > 0 ? it - S : 0;
+                    for (int j = first; j < it; ++j) {
+                        if (j == p.withhold && blockIdx.x == 0) continue;
+                        drain_wait(full_bar(j % S), static_cast<uint32_t>((j / S) & 1),
+                                   p.wait_limit_ns);
+                    }
+                } else {
+                    // The peer's copies complete on the leader's barriers, which this
+                    // CTA cannot wait on: give them a bounded grace period (a stage
+                    // lands within microseconds), then the closing cluster barrier
+                    // keeps this CTA alive until the leader has drained as well.
+                    const unsigned long long grace =
+                        p.wait_limit_ns < 200000ull ? p.wait_limit_ns : 200000ull;
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < grace) {
+                    }
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
+            // -------------------------------------------------------- MMA issuer
             const uint32_t a_base = smem_addr(a_ring);
             const uint32_t b_base = smem_addr(b_ring);
             // K-major operands: 128-byte rows, 8-row groups 1024 bytes apart; one
@@ -318,18 +387,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int it = 0;
             int lt = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++lt) {
+            for (int t = unit; ok && t < p.num_tiles; t += num_units, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
-                if (!bounded_wait(tempty_bar(acc), acc_ph ^ 1u, abort_flag, p.wait_limit_ns,
-                                  ROLE_MMA, it)) {
+                if (!bounded_wait<PAIR>(tempty_bar(acc), acc_ph ^ 1u, abort_flag, p.wait_limit_ns,
+                                        ROLE_MMA, it, peer_rank)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
-                    if (!bounded_wait(full_bar(s), ph, abort_flag, p.wait_limit_ns, ROLE_MMA, it)) {
+                    if (!bounded_wait<PAIR>(full_bar(s), ph, abort_flag, p.wait_limit_ns, ROLE_MMA,
+                                            it, peer_rank)) {
                         ok = false;
                         break;
                     }
@@ -340,9 +410,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = smem_desc(a_s + kk * 32u, 16u, 1024u);
                         const uint64_t bd = smem_desc(b_s + kk * b_kstep, b_lbo, 1024u);
-                        umma_f16(d_tmem, ad, bd, p.idesc, (kt | kk) != 0 ? 1u : 0u);
+                        const uint32_t accum = (kt | kk) != 0 ? 1u : 0u;
+                        if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
+                        else umma_f16(d_tmem, ad, bd, p.idesc, accum);
                     }
-                    umma_commit(empty_bar(s));  // slot s is free once these MMAs finish
+                    // slot s is free (in both CTAs) once these MMAs finish
+                    if constexpr (PAIR) umma_commit_pair_multicast(empty_bar(s), kPairMask);
+                    else umma_commit(empty_bar(s));
                     ++it;
                     if (++s == S) {
                         s = 0;
@@ -350,11 +424,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue (of both CTAs)
+                if constexpr (PAIR) umma_commit_pair_multicast(tfull_bar(acc), kPairMask);
+                else umma_commit(tfull_bar(acc));
             }
             if (!ok) {
                 // Wait for every MMA this thread issued before TMEM is freed.
-                umma_commit(drain_bar);
+                if constexpr (PAIR) umma_commit_pair_multicast(drain_bar, 0x1);
+                else umma_commit(drain_bar);
                 drain_wait(drain_bar, 0u, p.wait_limit_ns);
             }
         }
@@ -362,18 +439,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = 32 * q + lane;
+        const int row_in_tile = static_cast<int>(rank) * BM + 32 * q + lane;
+        const uint32_t tempty_leader0 = PAIR ? mapa_shared(tempty_bar(0), 0u) : tempty_bar(0);
         int lt = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+        for (int t = unit; t < p.num_tiles; t += num_units, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
-            if (!bounded_wait(tfull_bar(acc), acc_ph, abort_flag, p.wait_limit_ns, ROLE_EPILOGUE,
-                              lt))
+            if (!bounded_wait<PAIR>(tfull_bar(acc), acc_ph, abort_flag, p.wait_limit_ns,
+                                    ROLE_EPILOGUE, lt, peer_rank))
                 break;
             tc_fence_after();
             int tm, tn;
             tile_coords(p, t, tm, tn);
-            const int row = tm * BM + row_in_tile;
+            const int row = tm * TILE_M + row_in_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(acc * p.bn);
             for (int c = 0; c < p.bn; c += 16) {
@@ -384,14 +462,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (row < p.M && col0 < p.N) store_row_chunk(p, row, col0, r);
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
+                else mbar_arrive(tempty_bar(acc));
+            }
         }
     }
 
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // no remote arrive or multicast is still pending
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, tmem_cols);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, tmem_cols);
+        else tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
@@ -428,18 +512,6 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
-// The kernel's dynamic shared-memory limit is a per-device attribute.
-bool smem_attribute_set(int dev) {
-    static std::mutex mu;
-    static bool done[64] = {false};
-    std::lock_guard<std::mutex> g(mu);
-    if (dev < 0 || dev >= 64) return false;
-    if (!done[dev])
-        done[dev] = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024) == cudaSuccess;
-    return done[dev];
-}
-
 int device_sms(int dev) {
     static std::mutex mu;
     static int cache[64] = {0};
@@ -449,41 +521,97 @@ int device_sms(int dev) {
     return cache[dev];
 }
 
-}  // namespace
+// The kernels' dynamic shared-memory limit is a per-device attribute.
+bool smem_attribute(int dev, bool pair) {
+    static std::mutex mu;
+    static bool done[64][2] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return false;
+    if (!done[dev][pair]) {
+        cudaError_t e = pair ? cudaFuncSetAttribute(gemm_tc_kernel<true>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    227 * 1024)
+                             : cudaFuncSetAttribute(gemm_tc_kernel<false>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    227 * 1024);
+        done[dev][pair] = e == cudaSuccess;
+    }
+    return done[dev][pair];
+}
 
-int tc_launch(const TcLaunch& L, cudaStream_t stream) {
+void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid,
+                        size_t smem, cudaStream_t stream) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(grid);
+    cfg->blockDim = dim3(NUM_THREADS);
+    cfg->dynamicSmemBytes = smem;
+    cfg->stream = stream;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
+// Number of CTA pairs that can be resident at once for a given shared-memory
+// size (cached per device and size).
+int max_resident_pairs(int dev, size_t smem) {
+    static std::mutex mu;
+    static size_t key_smem[64][8] = {};
+    static int val[64][8] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    for (int i = 0; i < 8; ++i)
+        if (key_smem[dev][i] == smem && val[dev][i] > 0) return val[dev][i];
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pair_launch_config(&cfg, attr, 2, smem, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<true>, &cfg) != cudaSuccess) n = 0;
+    for (int i = 0; i < 8; ++i)
+        if (key_smem[dev][i] == 0 || i == 7) {
+            key_smem[dev][i] = smem;
+            val[dev][i] = n;
+            break;
+        }
+    return n;
+}
+
+struct Geometry {
+    int grid = 0;      // CTAs launched
+    int cluster = 1;   // CTAs per cluster
+    size_t smem = 0;   // dynamic shared memory per CTA
+    int units = 0;     // persistent workers (CTAs, or CTA pairs)
+};
+
+// Parameters and launch geometry of one call (no launch).
+int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
+    const bool pair = L.pair != 0;
     const int bn = L.tile_n;
     const int S = L.stages;
-    CUtensorMap tmA, tmB;
-    // A: M x K row-major, boxes of 64 (K) x 128 (M).
-    if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
-    if (L.b_col_major) {
-        // B column-major = N x K row-major: boxes of 64 (K) x bn (N).
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, bn)) return GEMM_ERR_LAUNCH;
-    } else {
-        // B row-major K x N: boxes of 64 (N) x 64 (K); bn/64 boxes per stage.
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
-    }
-
-    TcParams p;
+    const int b_cols = pair ? bn / 2 : bn;
+    const int tile_m = pair ? 2 * BM : BM;
     p.M = static_cast<int>(L.M);
     p.N = static_cast<int>(L.N);
     p.K = static_cast<int>(L.K);
-    p.tiles_m = static_cast<int>((L.M + BM - 1) / BM);
+    p.tiles_m = static_cast<int>((L.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<int>((L.N + bn - 1) / bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_tiles = static_cast<int>((L.K + BK - 1) / BK);
-    p.group_m = 16;
+    p.group_m = pair ? 8 : 16;
     p.stages = S;
     p.bn = bn;
     p.b_mn_major = L.b_col_major ? 0 : 1;
     p.out_bf16 = L.out_bf16;
     // Instruction descriptor (kind::f16): D fp32 (bit 4), A and B type
     // (bits 7..9, 10..12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B major
-    // (bit 16: 1 = MN-major), N >> 3 at bits 17..22, M >> 4 at bits 24..28.
+    // (bit 16: 1 = MN-major), N >> 3 at bits 17..22, M >> 4 at bits 24..28
+    // (M = 256 across a CTA pair).
     const uint32_t fmt = L.in_bf16 ? 1u : 0u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(p.b_mn_major) << 16) |
-              (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+              (static_cast<uint32_t>(bn >> 3) << 17) |
+              (static_cast<uint32_t>(tile_m >> 4) << 24);
     p.alpha = L.alpha;
     p.beta = L.beta;
     p.C = L.C;
@@ -495,15 +623,67 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
     const int sms = device_sms(dev);
     if (sms <= 0) return GEMM_ERR_CUDA;
+    if (!smem_attribute(dev, pair)) return GEMM_ERR_LAUNCH;
 
-    size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + bn * BK * 2) + sizeof(SharedCtl);
+    size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) + sizeof(SharedCtl);
     // A 256-wide tile uses all 512 TMEM columns: keep one CTA per SM.
     if (bn == 256 && smem < 120 * 1024) smem = 120 * 1024;
-    if (!smem_attribute_set(dev)) return GEMM_ERR_LAUNCH;
+    geo.smem = smem;
+    if (!pair) {
+        geo.cluster = 1;
+        geo.units = p.num_tiles < sms ? p.num_tiles : sms;
+        geo.grid = geo.units;
+    } else {
+        const int max_pairs = max_resident_pairs(dev, smem);
+        if (max_pairs <= 0) return GEMM_ERR_LAUNCH;
+        geo.cluster = 2;
+        geo.units = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
+        geo.grid = 2 * geo.units;
+    }
+    return GEMM_OK;
+}
 
-    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    gemm_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(tmA, tmB, p);
+}  // namespace
+
+int tc_launch(const TcLaunch& L, cudaStream_t stream) {
+    const bool pair = L.pair != 0;
+    const int bn = L.tile_n;
+    const int b_cols = pair ? bn / 2 : bn;
+    CUtensorMap tmA, tmB;
+    // A: M x K row-major, boxes of 64 (K) x 128 (M).
+    if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
+    if (L.b_col_major) {
+        // B column-major = N x K row-major: boxes of 64 (K) x b_cols (N).
+        if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
+    } else {
+        // B row-major K x N: boxes of 64 (N) x 64 (K); b_cols/64 boxes per stage.
+        if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
+    }
+    TcParams p;
+    Geometry geo;
+    const int st = plan(L, p, geo);
+    if (st != GEMM_OK) return st;
+    if (!pair) {
+        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, p);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, p) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {
+    TcParams p;
+    Geometry geo;
+    const int st = plan(L, p, geo);
+    if (st != GEMM_OK) return st;
+    if (grid) *grid = geo.grid;
+    if (cluster) *cluster = geo.cluster;
+    if (smem_bytes) *smem_bytes = static_cast<int>(geo.smem);
+    return GEMM_OK;
 }
 
 int tc_read_and_clear_status(GemmDeviceStatus* out) {

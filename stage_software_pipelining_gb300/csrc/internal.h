@@ -28,7 +28,8 @@ struct TcLaunch {
     int out_bf16;     // 0 fp32 output, 1 bf16 output
     int b_col_major;  // 0 B row-major (N contiguous), 1 B column-major (K contiguous)
     int stages;       // 1..6
-    int tile_n;       // 128 or 256
+    int tile_n;       // tile width: 128 or 256
+    int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256
     int64_t wait_limit_ns;
     int withhold_arrive;
 };
@@ -48,6 +49,9 @@ struct SimtLaunch {
 // Enqueue the tensor-core GEMM (K > 0, M > 0, N > 0, alpha != 0).  Returns a
 // gemm_status_t.
 int tc_launch(const TcLaunch& L, cudaStream_t stream);
+// Launch geometry tc_launch would use (CTAs, CTAs per cluster, dynamic
+// shared memory per CTA), without launching.
+int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes);
 // Read the device status word of the tensor-core kernel on the current device
 // and reset it to zero (synchronous).
 int tc_read_and_clear_status(GemmDeviceStatus* out);
@@ -58,8 +62,9 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream);
 int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,
                  cudaStream_t stream);
 
-constexpr int kTcMaxStages128 = 6;
-constexpr int kTcMaxStages256 = 4;
+constexpr int kTcMaxStages128 = 6;   // 128 x 128 tile: 32 KB per stage
+constexpr int kTcMaxStages256 = 4;   // 128 x 256 tile: 48 KB per stage
+constexpr int kTcMaxStagesPair = 6;  // 256 x 256 tile on a CTA pair: 32 KB per stage per CTA
 constexpr int kSimtMaxStages = 4;
 
 }  // namespace ssp

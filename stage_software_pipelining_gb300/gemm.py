@@ -25,9 +25,15 @@ GEMM_ERR_LAUNCH = -4
 GEMM_ERR_TIMEOUT = -5
 GEMM_ERR_CUDA = -6
 
+# Tensor-core tiles (gemm_tile_t)
+TILE_AUTO = 0
+TILE_128x128 = 128
+TILE_128x256 = 256
+TILE_256x256_2SM = 512
+
 # Every extern "C" symbol include/gemm.h declares.
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
-           "gemm_status_string", "gemm_max_stages", "gemm_debug_set")
+           "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set")
 
 _lock = threading.Lock()
 _lib = None
@@ -57,13 +63,14 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_checked.argtypes = base + [i32, i32, p]
         lib.gemm_host.argtypes = base + [i32, i32, p]
         for name in ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
-                     "gemm_max_stages", "gemm_debug_set"):
+                     "gemm_max_stages", "gemm_plan", "gemm_debug_set"):
             getattr(lib, name).restype = i32
         lib.gemm_host_release.argtypes = []
         lib.gemm_status_string.argtypes = [i32]
         lib.gemm_status_string.restype = ctypes.c_char_p
         lib.gemm_max_stages.argtypes = [i32, i32]
         lib.gemm_debug_set.argtypes = [i64, i32]
+        lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p, p, p]
         if path == LIB_PATH:
             _lib = lib
         return lib
@@ -129,12 +136,13 @@ def default_stages(dtype: int) -> int:
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
-         beta: float = 0.0, stages: int | None = None, tile_n: int = 0,
+         beta: float = 0.0, stages: int | None = None, tile: int = TILE_AUTO,
          stream: torch.cuda.Stream | None = None, checked: bool = False) -> torch.Tensor:
     """C = alpha*A@B + beta*C in place on the GPU (libgemm.so gemm_ex / gemm_checked).
 
     A: M x K row-major; B: K x N row-major, or column-major as a transposed
     view of an N x K tensor; C: M x N row-major, fp32 (or bf16 for bf16 inputs).
+    tile: a TILE_* code for the tensor-core path (0 on the SIMT path).
     Raises GemmError on a non-OK status.  Returns C.
     """
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
@@ -147,14 +155,14 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
     fn = lib.gemm_checked if checked else lib.gemm_ex
     with torch.cuda.device(C.device):
         status = fn(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
-                    float(alpha), float(beta), code, st, bcm, int(tile_n), s)
+                    float(alpha), float(beta), code, st, bcm, int(tile), s)
     if status != GEMM_OK:
         raise GemmError(status, "gemm_checked" if checked else "gemm_ex")
     return C
 
 
 def gemm_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
-              beta: float = 0.0, stages: int | None = None, tile_n: int = 0,
+              beta: float = 0.0, stages: int | None = None, tile: int = TILE_AUTO,
               stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """The same operation on HOST tensors (libgemm.so gemm_host): copies in,
     computes on the current device, copies C back, synchronises."""
@@ -166,7 +174,7 @@ def gemm_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 
     s = (stream or torch.cuda.current_stream()).cuda_stream
     status = load_library().gemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
                                       C.data_ptr(), ldc, float(alpha), float(beta), code, st,
-                                      bcm, int(tile_n), s)
+                                      bcm, int(tile), s)
     if status != GEMM_OK:
         raise GemmError(status, "gemm_host")
     return C
@@ -177,8 +185,19 @@ def raw_call(name: str, *args) -> int:
     return int(getattr(load_library(), name)(*args))
 
 
-def max_stages(dtype: int, tile_n: int = 0) -> int:
-    return int(load_library().gemm_max_stages(int(dtype), int(tile_n)))
+def max_stages(dtype: int, tile: int = TILE_AUTO) -> int:
+    return int(load_library().gemm_max_stages(int(dtype), int(tile)))
+
+
+def plan(M: int, N: int, K: int, dtype: int, stages: int, b_col_major: bool = False,
+         tile: int = TILE_AUTO) -> dict:
+    """Launch geometry of a call (libgemm.so gemm_plan); needs a CUDA device."""
+    grid, cluster, smem = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    st = load_library().gemm_plan(M, N, K, dtype, stages, int(b_col_major), tile,
+                                  ctypes.byref(grid), ctypes.byref(cluster), ctypes.byref(smem))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan")
+    return {"grid": grid.value, "cluster": cluster.value, "smem_bytes": smem.value}
 
 
 def debug_set(wait_limit_ns: int = 0, withhold_arrive: int = -1) -> None:

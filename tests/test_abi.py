@@ -49,11 +49,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def gemm_ex(lib, M, N, K, A=P, lda=None, B=P, ldb=None, C=P, ldc=None, alpha=1.0, beta=0.0,
-            dtype=GEMM_BF16_F32, stages=4, bcm=0, tile_n=0):
+            dtype=GEMM_BF16_F32, stages=4, bcm=0, tile=0):
     lda = K if lda is None else lda
     ldb = (K if bcm else N) if ldb is None else ldb
     ldc = N if ldc is None else ldc
-    return lib.gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, bcm, tile_n,
+    return lib.gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages, bcm, tile,
                        None)
 
 
@@ -69,10 +69,11 @@ def test_bad_dtype_and_stages(lib):
     assert gemm_ex(lib, 8, 8, 8, stages=0) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, stages=7) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=5) == G.GEMM_ERR_ARG
-    # 256-wide tiles hold at most 4 stages in shared memory
-    assert gemm_ex(lib, 8, 512, 8, stages=5, tile_n=256) == G.GEMM_ERR_UNSUPPORTED
-    assert gemm_ex(lib, 8, 8, 8, tile_n=192) == G.GEMM_ERR_ARG
-    assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile_n=128) == G.GEMM_ERR_ARG
+    # 128 x 256 tiles hold at most 4 stages in shared memory
+    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_128x256) == G.GEMM_ERR_UNSUPPORTED
+    assert gemm_ex(lib, 8, 8, 8, tile=192) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, tile=1024) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=128) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, bcm=2) == G.GEMM_ERR_ARG
 
 
@@ -129,8 +130,9 @@ def test_status_strings(lib):
 
 def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_F32, 0) == 4
-    assert lib.gemm_max_stages(GEMM_BF16_F32, 256) == 4
-    assert lib.gemm_max_stages(GEMM_BF16_F32, 128) == 6
+    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
+    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 6
+    assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 6
     assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 6
     assert lib.gemm_max_stages(GEMM_F32, 128) == G.GEMM_ERR_ARG
     assert lib.gemm_max_stages(9, 0) == G.GEMM_ERR_ARG

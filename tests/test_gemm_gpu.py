@@ -40,7 +40,7 @@ def workload(dtype, M, N, K, **kw):
     return dataclasses.replace(w, **kw) if kw else w
 
 
-def run_gpu(inp, stages, tile_n=0, alpha=None, beta=None, checked=True, guard=True):
+def run_gpu(inp, stages, tile=0, alpha=None, beta=None, checked=True, guard=True):
     """Run the CUDA path on padded device copies; return (host C as float64, guard)."""
     w = inp.workload
     alpha = w.alpha if alpha is None else alpha
@@ -52,7 +52,7 @@ def run_gpu(inp, stages, tile_n=0, alpha=None, beta=None, checked=True, guard=Tr
     gC = GuardedC(w.M, w.N, out_dt, init=init.cuda() if init is not None else None)
     if init is None:
         gC.view.fill_(float("nan") if beta == 0.0 else 0.0)
-    G.gemm(A, B, gC.view, alpha, beta, stages=stages, tile_n=tile_n, checked=checked)
+    G.gemm(A, B, gC.view, alpha, beta, stages=stages, tile=tile, checked=checked)
     torch.cuda.synchronize()
     if guard:
         gC.check()
@@ -103,16 +103,22 @@ def test_simt_stage_invariance_bitwise():
 
 
 # --------------------------------------------------------------------------- tensor cores
+TILES = [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM]
+TILE_STAGES = {G.TILE_128x128: [1, 2, 3, 4, 5, 6], G.TILE_128x256: [1, 2, 3, 4],
+               G.TILE_256x256_2SM: [1, 2, 3, 4, 5, 6]}
+
+
 @pytest.mark.parametrize("dtype", TC_DTYPES)
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("b_col_major", [False, True])
-def test_tc_ragged_matches_oracle(dtype, tile_n, b_col_major):
-    # several 128 x tile_n tiles with ragged M, N and K tails
+def test_tc_ragged_matches_oracle(dtype, tile, b_col_major):
+    # several tiles with ragged M, N and K tails (for the 256 x 256 pair tile
+    # the second tile row leaves the second CTA entirely out of range)
     w = workload(dtype, 300, 520, 200, b_col_major=b_col_major, beta=0.0)
     inp = make_inputs(w)
-    out, _ = run_gpu(inp, 4, tile_n=tile_n)
+    out, _ = run_gpu(inp, 4, tile=tile)
     ref, absb = oracle_full(inp)
-    check_against_oracle(out, ref, absb, dtype, what=f"tc dt={dtype} bn={tile_n} "
+    check_against_oracle(out, ref, absb, dtype, what=f"tc dt={dtype} tile={tile} "
                                                       f"colB={b_col_major}")
 
 
@@ -123,34 +129,38 @@ def test_tc_shape_fuzz(shape, b_col_major):
     M, N, K = shape
     for dtype in (GEMM_BF16_F32, GEMM_F16_F32):
         inp = make_inputs(workload(dtype, M, N, K, b_col_major=b_col_major, beta=0.0))
-        out, _ = run_gpu(inp, 3)
         ref, absb = oracle_full(inp)
-        check_against_oracle(out, ref, absb, dtype, what=f"tc fuzz {shape} dt={dtype}")
+        for tile in (G.TILE_AUTO, G.TILE_128x256, G.TILE_256x256_2SM):
+            out, _ = run_gpu(inp, 3, tile=tile)
+            check_against_oracle(out, ref, absb, dtype, what=f"tc fuzz {shape} dt={dtype} "
+                                                              f"tile={tile}")
 
 
-@pytest.mark.parametrize("tile_n,stages_list", [(128, [1, 2, 3, 4, 5, 6]), (256, [1, 2, 3, 4])])
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("dtype", TC_DTYPES)
-def test_tc_stage_invariance_bitwise(tile_n, stages_list, dtype):
+def test_tc_stage_invariance_bitwise(tile, dtype):
     """The ring depth changes timing only: every stage count gives the same bits."""
+    stages_list = TILE_STAGES[tile]
     w = workload(dtype, 384, 640, 520, beta=0.0)
     inp = make_inputs(w)
-    outs = {s: run_gpu(inp, s, tile_n=tile_n)[0] for s in stages_list}
+    outs = {s: run_gpu(inp, s, tile=tile)[0] for s in stages_list}
     ref, absb = oracle_full(inp)
     check_against_oracle(outs[stages_list[0]], ref, absb, dtype, what="tc invariance base")
     for s in stages_list[1:]:
         assert np.array_equal(outs[s], outs[stages_list[0]], equal_nan=True), \
-            f"stages={s} differs from stages={stages_list[0]} (tile_n={tile_n})"
+            f"stages={s} differs from stages={stages_list[0]} (tile={tile})"
 
 
 @pytest.mark.parametrize("alpha,beta", [(1.0, 1.0), (-0.5, 2.0), (2.0, -1.0), (0.25, 0.0)])
 @pytest.mark.parametrize("dtype", TC_DTYPES)
-def test_tc_alpha_beta(alpha, beta, dtype):
+@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM])
+def test_tc_alpha_beta(alpha, beta, dtype, tile):
     w = workload(dtype, 260, 300, 136, alpha=alpha, beta=beta)
     inp = make_inputs(w)
     if inp.C0 is None and beta != 0.0:
         gen = torch.Generator().manual_seed(99)
         inp.C0 = (torch.rand(260, 300, generator=gen) * 2 - 1).to(OUT_DTYPE[dtype])
-    out, _ = run_gpu(inp, 2, alpha=alpha, beta=beta)
+    out, _ = run_gpu(inp, 2, tile=tile, alpha=alpha, beta=beta)
     ref, absb = oracle_full(inp, alpha, beta)
     check_against_oracle(out, ref, absb, dtype, beta=beta, C0=inp.C0,
                          what=f"alpha={alpha} beta={beta}")
@@ -194,7 +204,8 @@ def test_empty_m_or_n_is_a_noop():
 
 
 # --------------------------------------------------------------------------- fault path
-def test_withheld_arrive_times_out_and_context_survives():
+@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM])
+def test_withheld_arrive_times_out_and_context_survives(tile):
     """Block 0's producer skips one stage: the MMA wait must run out, the
     kernel must return GEMM_ERR_TIMEOUT (no hang, no trap), and the next
     GEMM on the same context must be correct."""
@@ -205,11 +216,11 @@ def test_withheld_arrive_times_out_and_context_survives():
     try:
         G.debug_set(50_000_000, 3)      # 50 ms per wait; withhold K tile 3
         with pytest.raises(G.GemmError) as e:
-            G.gemm(A, B, C, stages=2, checked=True)
+            G.gemm(A, B, C, stages=2, tile=tile, checked=True)
         assert e.value.status == G.GEMM_ERR_TIMEOUT
     finally:
         G.debug_set(0, -1)
-    G.gemm(A, B, C, stages=2, checked=True)
+    G.gemm(A, B, C, stages=2, tile=tile, checked=True)
     ref, absb = oracle_full(inp)
     check_against_oracle(C.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
                          what="after timeout")
@@ -238,13 +249,15 @@ def sample_indices(M, N, count, seed):
     return np.array(rows), np.array(cols)
 
 
-@pytest.mark.parametrize("name,stages,tile_n", [
+@pytest.mark.parametrize("name,stages,tile", [
     ("fp32_2048", 2, 0),
     ("fp16_2048", 4, 0),
-    ("bf16_8192_beta1", 4, 256),
-    ("bf16_ragged_colB", 4, 256),
+    ("bf16_8192_beta1", 4, G.TILE_128x256),
+    ("bf16_8192_beta1", 6, G.TILE_256x256_2SM),
+    ("bf16_ragged_colB", 4, G.TILE_128x256),
+    ("bf16_ragged_colB", 6, G.TILE_256x256_2SM),
 ])
-def test_full_size_workload_sampled(name, stages, tile_n):
+def test_full_size_workload_sampled(name, stages, tile):
     w = BY_NAME[name]
     inp = make_inputs(w)
     A = inp.A.cuda()
@@ -252,7 +265,7 @@ def test_full_size_workload_sampled(name, stages, tile_n):
     assert (B.stride(0) == 1) == w.b_col_major
     C = inp.C0.cuda() if inp.C0 is not None else torch.full((w.M, w.N), float("nan"),
                                                             dtype=OUT_DTYPE[w.dtype], device="cuda")
-    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile_n=tile_n, checked=True)
+    G.gemm(A, B, C, w.alpha, w.beta, stages=stages, tile=tile, checked=True)
     rows, cols = sample_indices(w.M, w.N, 3000, 7)
     got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
     ref, absb = oracle.gemm_entries(inp.A, inp.B, inp.C0, w.alpha, w.beta, rows=rows, cols=cols)
@@ -261,25 +274,25 @@ def test_full_size_workload_sampled(name, stages, tile_n):
     if w.dtype == GEMM_BF16_BF16:
         # Frobenius criterion on the fp32-output launch of the same kernel
         C32 = torch.empty(w.M, w.N, device="cuda")
-        G.gemm(A, B, C32, w.alpha, 0.0, stages=stages, tile_n=tile_n, checked=True)
+        G.gemm(A, B, C32, w.alpha, 0.0, stages=stages, tile=tile, checked=True)
         got32 = C32[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
         check_against_oracle(got32.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
                              what=name + " fp32 twin")
 
 
 def test_full_size_stage_sweep_is_bitwise_invariant():
-    """At the 8192^3 bf16 size, every stage count of the 128-wide tile and of
-    the 256-wide tile gives identical bits (the sweep the benchmark times)."""
+    """At the 8192^3 bf16 size, every stage count of each tile gives identical
+    bits (the sweep the benchmark times)."""
     w = BY_NAME["bf16_8192_beta1"]
     inp = make_inputs(w)
     A, B = inp.A.cuda(), inp.B.cuda()
     C0 = inp.C0.cuda()
-    for tile_n, stages in ((128, (1, 2, 3, 4, 5, 6)), (256, (1, 2, 3, 4))):
+    for tile in TILES:
         base = None
-        for s in stages:
+        for s in TILE_STAGES[tile]:
             C = C0.clone()
-            G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile_n=tile_n, checked=True)
+            G.gemm(A, B, C, w.alpha, w.beta, stages=s, tile=tile, checked=True)
             if base is None:
                 base = C
             else:
-                assert torch.equal(C, base), f"tile_n={tile_n} stages={s}"
+                assert torch.equal(C, base), f"tile={tile} stages={s}"
