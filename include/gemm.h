@@ -84,6 +84,14 @@ typedef enum {
     GEMM_TILE_256x256_2SM = 512  /* a CTA pair, stages 1..6 (32 KB per stage per CTA) */
 } gemm_tile_t;
 
+/* Register-fragment scheme of the SIMT sgemm (gemm_ex's `tile` when dtype
+ * is GEMM_F32): fragments double-buffered in registers (the warp-scope
+ * double buffer, the default) or a single fragment set. */
+typedef enum {
+    GEMM_SIMT_FRAGMENTS_DOUBLE = 0,
+    GEMM_SIMT_FRAGMENTS_SINGLE = 1
+} gemm_simt_fragments_t;
+
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_ARG = -1,          /* bad size, leading dimension, pointer, dtype or stages */
@@ -115,9 +123,9 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void
  *   b_col_major  0: B row-major (as gemm); 1: B column-major (element (k,j)
  *                at B[j*ldb + k], ldb >= K).  Column-major B is implemented on
  *                the tensor-core path only (GEMM_ERR_UNSUPPORTED for GEMM_F32).
- *   tile         a gemm_tile_t (tensor-core path); a stage count above the
- *                tile's limit gives GEMM_ERR_UNSUPPORTED.  Must be 0 on the
- *                SIMT path (its tile is 128 x 64).
+ *   tile         tensor-core path: a gemm_tile_t; a stage count above the
+ *                tile's limit gives GEMM_ERR_UNSUPPORTED.  SIMT path (tile
+ *                128 x 64): a gemm_simt_fragments_t.
  */
 int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
             int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
@@ -163,6 +171,24 @@ int gemm_max_stages(int dtype, int tile);
  */
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_major, int tile,
               int* grid, int* cluster, int* smem_bytes);
+
+/*
+ * pipelined_copy -- dst[0 .. n_bytes) = src[0 .. n_bytes), streamed through a
+ * ring of `stages` shared-memory slots per thread (asynchronous 16-byte
+ * copies, grid-stride), asynchronous on `stream`.
+ *
+ * This is the bandwidth-bound counter-example to the GEMM: the grid-stride
+ * copy through a `cuda::pipeline` of "learn-kernels.com, Matrix
+ * multiplication" (the listing after "Overlap needs stages"), which
+ * "Software Pipelining and Double Buffering" ("When it pays") and the CUDA
+ * Handbook ("Asynchronous data movement", closing rule) name as the case
+ * where extra stages do not pay.  Its stage sweep is measured by bench.py.
+ *   dst, src   device pointers, 16-byte aligned, ranges must not overlap
+ *              (GEMM_ERR_ARG), owned by the caller
+ *   n_bytes    >= 0, a multiple of 16 (GEMM_ERR_ALIGN otherwise); 0 is a no-op
+ *   stages     1..8 (GEMM_ERR_ARG otherwise)
+ */
+int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void* stream);
 
 /*
  * gemm_debug_set -- test hook for the bounded waits (not thread-safe; affects

@@ -69,6 +69,8 @@ def _open(path: str):
     lib.oracle_decode_f32.restype = f64
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
+    lib.oracle_copy_bytes.argtypes = [p, p, i64]
+    lib.oracle_copy_bytes.restype = i32
     return lib
 
 
@@ -227,6 +229,16 @@ def gemm_entries(A, B, C0=None, alpha: float = 1.0, beta: float = 0.0, *, rows, 
     if st != 0:
         raise RuntimeError(f"oracle_gemm_entries failed with status {st}")
     return out, absv
+
+
+def copy_bytes(src: np.ndarray) -> np.ndarray:
+    """The streaming copy's result: a byte-for-byte copy of src (uint8)."""
+    src = np.ascontiguousarray(np.asarray(src, dtype=np.uint8))
+    out = np.empty_like(src)
+    st = _load().oracle_copy_bytes(out.ctypes.data, src.ctypes.data, src.size)
+    if st != 0:
+        raise RuntimeError(f"oracle_copy_bytes failed with status {st}")
+    return out
 
 
 def decode_f16(bits: int) -> float:

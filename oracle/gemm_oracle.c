@@ -246,6 +246,17 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K,
     return ORACLE_OK;
 }
 
+/*
+ * The streaming-copy counter-example (the grid-stride copy of
+ * "learn-kernels.com, Matrix multiplication", listing after "Overlap needs
+ * stages"): its result is defined as byte i of dst = byte i of src.
+ */
+int oracle_copy_bytes(unsigned char* dst, const unsigned char* src, int64_t n) {
+    if (n < 0 || (n > 0 && (dst == NULL || src == NULL))) return ORACLE_EARG;
+    for (int64_t i = 0; i < n; ++i) dst[i] = src[i];
+    return ORACLE_OK;
+}
+
 /* Threads an OpenMP region would use with nthreads <= 0 (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -70,7 +70,8 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, c
         if (stages < 1 || stages > ssp::kTcMaxStages128) return {GEMM_ERR_ARG, 0};
         if (stages > tile_max_stages(r.tile)) return {GEMM_ERR_UNSUPPORTED, 0};
     } else {
-        if (tile != 0) return {GEMM_ERR_ARG, 0};
+        if (tile != GEMM_SIMT_FRAGMENTS_DOUBLE && tile != GEMM_SIMT_FRAGMENTS_SINGLE)
+            return {GEMM_ERR_ARG, 0};
         if (stages < 1 || stages > ssp::kSimtMaxStages) return {GEMM_ERR_ARG, 0};
     }
     const bool use_a = M > 0 && K > 0;
@@ -128,7 +129,7 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     if (dtype == GEMM_F32) {
         ssp::SimtLaunch L{M, N, K, static_cast<const float*>(A), lda,
                           static_cast<const float*>(B), ldb, static_cast<float*>(C), ldc,
-                          alpha, beta, stages};
+                          alpha, beta, stages, tile == GEMM_SIMT_FRAGMENTS_SINGLE};
         return ssp::simt_launch(L, stream);
     }
     const ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
@@ -253,7 +254,10 @@ const char* gemm_status_string(int status) {
 }
 
 int gemm_max_stages(int dtype, int tile) {
-    if (dtype == GEMM_F32) return tile == 0 ? ssp::kSimtMaxStages : GEMM_ERR_ARG;
+    if (dtype == GEMM_F32)
+        return (tile == GEMM_SIMT_FRAGMENTS_DOUBLE || tile == GEMM_SIMT_FRAGMENTS_SINGLE)
+                   ? ssp::kSimtMaxStages
+                   : GEMM_ERR_ARG;
     if (!is_tc(dtype)) return GEMM_ERR_ARG;
     if (tile == GEMM_TILE_AUTO) return ssp::kTcMaxStages128;
     const int m = tile_max_stages(tile);
@@ -288,6 +292,17 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_
     const ssp::TcLaunch L = tc_request(M, N, K, P, lda, P, ldb, const_cast<void*>(P), ldc, 1.0f,
                                        0.0f, dtype, stages, b_col_major, v.tile);
     return ssp::tc_plan(L, grid, cluster, smem_bytes);
+}
+
+int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void* stream) {
+    if (n_bytes < 0 || stages < 1 || stages > ssp::kCopyMaxStages) return GEMM_ERR_ARG;
+    if (n_bytes == 0) return GEMM_OK;
+    if (dst == nullptr || src == nullptr) return GEMM_ERR_ARG;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + static_cast<uintptr_t>(n_bytes) && s < d + static_cast<uintptr_t>(n_bytes))
+        return GEMM_ERR_ARG;  // overlapping ranges
+    if (!aligned16(dst) || !aligned16(src) || n_bytes % 16 != 0) return GEMM_ERR_ALIGN;
+    return ssp::copy_launch(dst, src, n_bytes, stages, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive) {

@@ -43,7 +43,8 @@ struct SimtLaunch {
     float* C;
     int64_t ldc;
     float alpha, beta;
-    int stages;  // 1..4
+    int stages;            // 1..4
+    int single_fragments;  // 1: one register fragment set; 0: two (double-buffered)
 };
 
 // Enqueue the tensor-core GEMM (K > 0, M > 0, N > 0, alpha != 0).  Returns a
@@ -61,6 +62,11 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream);
 // C = beta*C over an M x N block (K == 0 or alpha == 0); elem_bytes 4 (fp32) or 2 (bf16).
 int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,
                  cudaStream_t stream);
+
+// Streaming copy of n_bytes (a multiple of 16) through a ring of `stages`
+// shared-memory slots per thread (1..8).
+int copy_launch(void* dst, const void* src, int64_t n_bytes, int stages, cudaStream_t stream);
+constexpr int kCopyMaxStages = 8;
 
 constexpr int kTcMaxStages128 = 6;   // 128 x 128 tile: 32 KB per stage
 constexpr int kTcMaxStages256 = 4;   // 128 x 256 tile: 48 KB per stage

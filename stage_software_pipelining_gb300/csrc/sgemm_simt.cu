@@ -85,8 +85,10 @@ __device__ __forceinline__ void load_tile(const SimtParams& p, int m0, int n0, i
 // acc[r][j] += A[ty + 16 r][k] * B[k][col(j)] over the BK values of one stage.
 // Thread rows are ty, ty+16, ..., ty+112; thread columns are 4tx..4tx+3 and
 // 32+4tx..32+4tx+3, so a warp's fragment reads hit distinct banks.
-__device__ __forceinline__ void compute_tile(const float* As, const float* Bs, int ty, int tx,
-                                             float (&acc)[8][8]) {
+// One fragment set: the A fragments of 4 consecutive k (8 float4) and the B
+// fragment of one k (2 float4) are loaded, then used.
+__device__ __forceinline__ void compute_tile_single(const float* As, const float* Bs, int ty,
+                                                    int tx, float (&acc)[8][8]) {
 #pragma unroll
     for (int kq = 0; kq < BK; kq += 4) {
         float4 a4[8];
@@ -108,7 +110,53 @@ __device__ __forceinline__ void compute_tile(const float* As, const float* Bs, i
     }
 }
 
-template <int STAGES>
+// Two fragment sets in registers (the warp-scope double buffer of
+// "CUTLASS-CuTe 初步(6)" section 6 and of "learn-kernels.com, Matrix
+// multiplication"): while the outer products of step k run, the B fragment of
+// step k+1 and, at the first step of each group of 4, the A fragments of the
+// next group are already being fetched from shared memory.
+__device__ __forceinline__ void compute_tile_double(const float* As, const float* Bs, int ty,
+                                                    int tx, float (&acc)[8][8]) {
+    float4 a4[2][8];
+    float4 bf[2][2];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        a4[0][r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD);
+    bf[0][0] = *reinterpret_cast<const float4*>(Bs + 4 * tx);
+    bf[0][1] = *reinterpret_cast<const float4*>(Bs + 32 + 4 * tx);
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+        const int kq = k >> 2, kk = k & 3;
+        if (kk == 0 && k + 4 < BK) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                a4[(kq + 1) & 1][r] =
+                    *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD + k + 4);
+        }
+        if (k + 1 < BK) {
+            bf[(k + 1) & 1][0] = *reinterpret_cast<const float4*>(Bs + (k + 1) * BN + 4 * tx);
+            bf[(k + 1) & 1][1] = *reinterpret_cast<const float4*>(Bs + (k + 1) * BN + 32 + 4 * tx);
+        }
+        const float4 b0 = bf[k & 1][0], b1 = bf[k & 1][1];
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float4 av = a4[kq & 1][r];
+            const float a = kk == 0 ? av.x : kk == 1 ? av.y : kk == 2 ? av.z : av.w;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(a, b[j], acc[r][j]);
+        }
+    }
+}
+
+template <bool FRAG_DB>
+__device__ __forceinline__ void compute_tile(const float* As, const float* Bs, int ty, int tx,
+                                             float (&acc)[8][8]) {
+    if constexpr (FRAG_DB) compute_tile_double(As, Bs, ty, tx, acc);
+    else compute_tile_single(As, Bs, ty, tx, acc);
+}
+
+template <int STAGES, bool FRAG_DB>
 __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p) {
     extern __shared__ __align__(16) float smem[];
     float* As = smem;                              // [STAGES][BM][A_LD]
@@ -130,7 +178,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
             cp_async_commit();
             cp_async_wait<0>();
             __syncthreads();  // read after write: every thread's copies landed
-            compute_tile(As, Bs, ty, tx, acc);
+            compute_tile<FRAG_DB>(As, Bs, ty, tx, acc);
             __syncthreads();  // write after read: nobody still reads the buffer
         }
     } else {
@@ -149,7 +197,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
             }
             cp_async_commit();
             const int cs = kt % STAGES;
-            compute_tile(As + cs * A_STAGE_FLOATS, Bs + cs * B_STAGE_FLOATS, ty, tx, acc);
+            compute_tile<FRAG_DB>(As + cs * A_STAGE_FLOATS, Bs + cs * B_STAGE_FLOATS, ty, tx, acc);
         }
         cp_async_wait<0>();
     }
@@ -190,7 +238,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     }
 }
 
-template <int S>
+template <int S, bool FRAG_DB>
 int launch_stages(const SimtParams& p, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(S) * (A_STAGE_FLOATS + B_STAGE_FLOATS) * sizeof(float);
     if (smem > 48 * 1024) {
@@ -201,14 +249,15 @@ int launch_stages(const SimtParams& p, cudaStream_t stream) {
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
         std::lock_guard<std::mutex> g(mu);
         if (!done[dev]) {
-            if (cudaFuncSetAttribute(sgemm_simt_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(sgemm_simt_kernel<S, FRAG_DB>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)) != cudaSuccess)
                 return GEMM_ERR_LAUNCH;
             done[dev] = true;
         }
     }
     dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
-    sgemm_simt_kernel<S><<<grid, THREADS, smem, stream>>>(p);
+    sgemm_simt_kernel<S, FRAG_DB><<<grid, THREADS, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
@@ -244,11 +293,20 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
     p.alpha = L.alpha;
     p.beta = L.beta;
     if ((p.M + BM - 1) / BM > 65535) return GEMM_ERR_UNSUPPORTED;
+    if (L.single_fragments) {
+        switch (L.stages) {
+            case 1: return launch_stages<1, false>(p, stream);
+            case 2: return launch_stages<2, false>(p, stream);
+            case 3: return launch_stages<3, false>(p, stream);
+            case 4: return launch_stages<4, false>(p, stream);
+            default: return GEMM_ERR_ARG;
+        }
+    }
     switch (L.stages) {
-        case 1: return launch_stages<1>(p, stream);
-        case 2: return launch_stages<2>(p, stream);
-        case 3: return launch_stages<3>(p, stream);
-        case 4: return launch_stages<4>(p, stream);
+        case 1: return launch_stages<1, true>(p, stream);
+        case 2: return launch_stages<2, true>(p, stream);
+        case 3: return launch_stages<3, true>(p, stream);
+        case 4: return launch_stages<4, true>(p, stream);
         default: return GEMM_ERR_ARG;
     }
 }

@@ -31,9 +31,14 @@ TILE_128x128 = 128
 TILE_128x256 = 256
 TILE_256x256_2SM = 512
 
+# SIMT register-fragment schemes (gemm_simt_fragments_t), passed as `tile` for fp32
+SIMT_FRAGMENTS_DOUBLE = 0
+SIMT_FRAGMENTS_SINGLE = 1
+
 # Every extern "C" symbol include/gemm.h declares.
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
-           "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set")
+           "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
+           "pipelined_copy")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +76,8 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_max_stages.argtypes = [i32, i32]
         lib.gemm_debug_set.argtypes = [i64, i32]
         lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p, p, p]
+        lib.pipelined_copy.argtypes = [p, p, i64, i32, p]
+        lib.pipelined_copy.restype = i32
         if path == LIB_PATH:
             _lib = lib
         return lib
@@ -142,7 +149,8 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
 
     A: M x K row-major; B: K x N row-major, or column-major as a transposed
     view of an N x K tensor; C: M x N row-major, fp32 (or bf16 for bf16 inputs).
-    tile: a TILE_* code for the tensor-core path (0 on the SIMT path).
+    tile: a TILE_* code for the tensor-core path; a SIMT_FRAGMENTS_* code on the
+    fp32 SIMT path.
     Raises GemmError on a non-OK status.  Returns C.
     """
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
@@ -198,6 +206,25 @@ def plan(M: int, N: int, K: int, dtype: int, stages: int, b_col_major: bool = Fa
     if st != GEMM_OK:
         raise GemmError(st, "gemm_plan")
     return {"grid": grid.value, "cluster": cluster.value, "smem_bytes": smem.value}
+
+
+def pipelined_copy(dst: torch.Tensor, src: torch.Tensor, stages: int = 2,
+                   stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dst[:] = src[:] byte for byte (libgemm.so pipelined_copy); both CUDA
+    tensors, contiguous, the same number of bytes (a multiple of 16)."""
+    if dst.device.type != "cuda" or src.device.type != "cuda":
+        raise ValueError("pipelined_copy takes CUDA tensors")
+    if not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("pipelined_copy takes contiguous tensors")
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("dst and src differ in size")
+    s = (stream or torch.cuda.current_stream(dst.device)).cuda_stream
+    with torch.cuda.device(dst.device):
+        st = load_library().pipelined_copy(dst.data_ptr(), src.data_ptr(), n, int(stages), s)
+    if st != GEMM_OK:
+        raise GemmError(st, "pipelined_copy")
+    return dst
 
 
 def debug_set(wait_limit_ns: int = 0, withhold_arrive: int = -1) -> None:

@@ -31,7 +31,7 @@ def lib():
 def declared_functions():
     text = open(HEADER, encoding="utf-8").read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_binding_exports():
@@ -74,6 +74,7 @@ def test_bad_dtype_and_stages(lib):
     assert gemm_ex(lib, 8, 8, 8, tile=192) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, tile=1024) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=128) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=2) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, bcm=2) == G.GEMM_ERR_ARG
 
 
@@ -130,6 +131,7 @@ def test_status_strings(lib):
 
 def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_F32, 0) == 4
+    assert lib.gemm_max_stages(GEMM_F32, 1) == 4      # single register fragment set
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 6
     assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 6
@@ -171,3 +173,15 @@ def test_ctypes_signatures_cover_exports(lib):
     for name in G.EXPORTS:
         fn = getattr(lib, name)
         assert fn.restype in (ctypes.c_int, ctypes.c_char_p), name
+
+
+def test_pipelined_copy_argument_checks(lib):
+    c = lib.pipelined_copy
+    assert c(P, P + 4096, 0, 2, None) == G.GEMM_OK          # empty: nothing touched
+    assert c(P, P + 4096, -16, 2, None) == G.GEMM_ERR_ARG
+    assert c(P, P + 4096, 64, 0, None) == G.GEMM_ERR_ARG
+    assert c(P, P + 4096, 64, 9, None) == G.GEMM_ERR_ARG
+    assert c(None, P, 64, 2, None) == G.GEMM_ERR_ARG
+    assert c(P, P + 32, 64, 2, None) == G.GEMM_ERR_ARG       # overlapping ranges
+    assert c(P + 8, P + 4096, 64, 2, None) == G.GEMM_ERR_ALIGN
+    assert c(P, P + 4096, 40, 2, None) == G.GEMM_ERR_ALIGN   # not a multiple of 16

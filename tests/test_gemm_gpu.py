@@ -102,6 +102,18 @@ def test_simt_stage_invariance_bitwise():
         assert np.array_equal(o, outs[0]), f"SIMT stages={s} differs from stages=1"
 
 
+@pytest.mark.parametrize("stages", [1, 2, 3, 4])
+def test_simt_register_fragment_schemes_agree_bitwise(stages):
+    """Double-buffered and single register fragments accumulate in the same
+    order, so they give the same bits; both match the oracle."""
+    inp = make_inputs(workload(GEMM_F32, 301, 198, 150))
+    dbl, _ = run_gpu(inp, stages, tile=G.SIMT_FRAGMENTS_DOUBLE)
+    single, _ = run_gpu(inp, stages, tile=G.SIMT_FRAGMENTS_SINGLE)
+    assert np.array_equal(dbl, single)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(dbl, ref, absb, GEMM_F32, what=f"simt fragments s={stages}")
+
+
 # --------------------------------------------------------------------------- tensor cores
 TILES = [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM]
 TILE_STAGES = {G.TILE_128x128: [1, 2, 3, 4, 5, 6], G.TILE_128x256: [1, 2, 3, 4],

@@ -483,3 +483,17 @@ def test_gcc_available():
 
 if __name__ == "__main__":
     sys.exit(min(run_pins_against(sys.argv[1]), 100))
+
+
+# ----------------------------------------------------------------------------- streaming copy
+def test_copy_oracle_is_byte_identity():
+    """The streaming copy's definition: byte i of the output is byte i of the
+    input (checked against numpy's own copy and the input itself)."""
+    rng = np.random.default_rng(23)
+    for n in (0, 1, 15, 16, 4096 + 7):
+        src = rng.integers(0, 256, n, dtype=np.uint8)
+        out = oracle.copy_bytes(src)
+        assert out.dtype == np.uint8 and out.shape == src.shape
+        assert np.array_equal(out, src.copy())
+        if n:
+            assert out.ctypes.data != src.ctypes.data
