@@ -173,6 +173,26 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_
               int* grid, int* cluster, int* smem_bytes);
 
 /*
+ * gemm_schedule_set -- how the tensor-core kernel spreads output tiles over
+ * its persistent CTAs (or CTA pairs), for the calls that follow from this
+ * process (not thread-safe):
+ *   0  automatic (default): currently the same as 1 (measured faster on
+ *      GB300 for every workload of this library).
+ *   1  whole tiles, round-robin over the units; no workspace.
+ *   2  stream-K tail: when the last round of whole tiles would leave units
+ *      idle, the leftover tiles are cut along K into segments spread evenly
+ *      over all units; the unit holding a tile's first K segment adds the
+ *      others' fp32 partials (in a fixed order) and writes C.  The partials
+ *      go to a workspace the library allocates with cudaMalloc on first use,
+ *      one per (device, stream), of at most one tile per unit (about 20 MB on
+ *      GB300).  Calls that overlap on the GPU must use different streams.
+ * Results are within the same tolerances for every schedule and, for one
+ * schedule, bit-identical for every stage count.  Returns GEMM_ERR_ARG for
+ * another value.
+ */
+int gemm_schedule_set(int schedule);
+
+/*
  * pipelined_copy -- dst[0 .. n_bytes) = src[0 .. n_bytes), streamed through a
  * ring of `stages` shared-memory slots per thread (asynchronous 16-byte
  * copies, grid-stride), asynchronous on `stream`.

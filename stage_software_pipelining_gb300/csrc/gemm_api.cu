@@ -14,6 +14,7 @@ namespace {
 
 int64_t g_wait_limit_ns = 2000000000LL;  // 2 s per pipeline wait
 int g_withhold_arrive = -1;
+int g_schedule = 0;  // tensor-core tile schedule (gemm_schedule_set)
 
 bool is_tc(int dtype) {
     return dtype == GEMM_F16_F32 || dtype == GEMM_BF16_F32 || dtype == GEMM_BF16_BF16;
@@ -115,6 +116,7 @@ ssp::TcLaunch tc_request(int64_t M, int64_t N, int64_t K, const void* A, int64_t
     L.pair = tile == GEMM_TILE_256x256_2SM;
     L.wait_limit_ns = g_wait_limit_ns;
     L.withhold_arrive = g_withhold_arrive;
+    L.schedule = g_schedule;
     return L;
 }
 
@@ -186,7 +188,11 @@ int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     ssp::GemmDeviceStatus ds;
     st = ssp::tc_read_and_clear_status(&ds);
     if (st != GEMM_OK) return st;
-    return ds.code != 0 ? GEMM_ERR_TIMEOUT : GEMM_OK;
+    if (ds.code != 0) {
+        ssp::tc_clear_workspace_flags();  // a run that gave up may leave flags set
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
 }
 
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
@@ -303,6 +309,12 @@ int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void
         return GEMM_ERR_ARG;  // overlapping ranges
     if (!aligned16(dst) || !aligned16(src) || n_bytes % 16 != 0) return GEMM_ERR_ALIGN;
     return ssp::copy_launch(dst, src, n_bytes, stages, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_schedule_set(int schedule) {
+    if (schedule < 0 || schedule > 2) return GEMM_ERR_ARG;
+    g_schedule = schedule;
+    return GEMM_OK;
 }
 
 int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive) {

@@ -41,7 +41,9 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/gemm.h"
 #include "internal.h"
@@ -75,6 +77,23 @@ struct TcParams {
     long long ldc;
     unsigned long long wait_limit_ns;
     int withhold;
+    // Stream-K tail: tiles [dp_tiles, num_tiles) are cut into K segments
+    // spread evenly over the persistent units (sk_iters = their k-tiles).
+    int dp_tiles;
+    long long sk_iters;
+    float* ws;              // one partial tile per unit (per CTA: 128 x bn fp32)
+    unsigned int* ws_flag;  // per unit and CTA rank: 1 = partial published
+};
+
+// One piece of work of a persistent unit: k-tiles [kb, ke) of a tile.
+//   FULL     the whole K range: the epilogue writes C
+//   PARTIAL  a later K segment of a stream-K tile: the epilogue publishes the
+//            fp32 partial in the unit's workspace slot
+//   FINISH   the K segment that starts at k = 0: the epilogue adds the
+//            partials of units [slot_lo, slot_hi) in order, then writes C
+enum JobRole { JOB_FULL = 0, JOB_PARTIAL = 1, JOB_FINISH = 2 };
+struct Job {
+    int tile, kb, ke, role, slot_lo, slot_hi;
 };
 
 struct SharedCtl {
@@ -82,6 +101,7 @@ struct SharedCtl {
     unsigned long long bar[2 * kTcMaxStages128 + 5];
     uint32_t tmem_base;
     int abort;
+    int epi_ok[2];  // the epilogue's per-job go/abort decision, by job parity
 };
 
 // Shared-memory matrix descriptor for tcgen05 with 128-byte swizzle:
@@ -152,6 +172,75 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& tm, i
     const int r = t - g * per_group;
     tm = first_m + r % gsize;
     tn = r / gsize;
+}
+
+// First stream-K iteration of unit u: floor(u * W / U).
+__device__ __forceinline__ long long sk_begin(const TcParams& p, int u, int U) {
+    return static_cast<long long>(u) * p.sk_iters / U;
+}
+
+// The unit whose stream-K range holds iteration g.
+__device__ __forceinline__ int sk_unit_of(const TcParams& p, long long g, int U) {
+    int u = static_cast<int>((g * U) / p.sk_iters);
+    while (u + 1 < U && sk_begin(p, u + 1, U) <= g) ++u;
+    while (u > 0 && sk_begin(p, u, U) > g) --u;
+    return u;
+}
+
+// The j-th job of unit u (false when it has no more).  Full tiles first (data
+// parallel, tile u + i*U), then at most two stream-K segments.  A unit's range
+// is shorter than one tile's K, so it touches at most two tiles; its
+// non-finishing segment (if any) comes first, so no unit waits before it has
+// published its own partial.
+__device__ bool next_job(const TcParams& p, int u, int U, int j, Job& job) {
+    const int n_dp = p.dp_tiles > u ? (p.dp_tiles - u + U - 1) / U : 0;
+    if (j < n_dp) {
+        job = {u + j * U, 0, p.k_tiles, JOB_FULL, 0, 0};
+        return true;
+    }
+    if (p.sk_iters == 0) return false;
+    const long long g0 = sk_begin(p, u, U), g1 = sk_begin(p, u + 1, U);
+    if (g0 == g1) return false;
+    const int KT = p.k_tiles;
+    const long long ta = g0 / KT, tb = (g1 - 1) / KT;
+    int js = j - n_dp;
+    if (ta != tb) {  // tail of tile ta (published), then head of tile tb (finished)
+        if (js == 0) {
+            job = {p.dp_tiles + static_cast<int>(ta), static_cast<int>(g0 % KT), KT, JOB_PARTIAL,
+                   0, 0};
+            return true;
+        }
+        js -= 1;
+        if (js != 0) return false;
+        const int ke = static_cast<int>((g1 - 1) % KT) + 1;
+        const int last = sk_unit_of(p, (tb + 1) * KT - 1, U);
+        job = {p.dp_tiles + static_cast<int>(tb), 0, ke, JOB_FINISH, u + 1, last + 1};
+        return true;
+    }
+    if (js != 0) return false;
+    const int kb = static_cast<int>(g0 % KT), ke = static_cast<int>((g1 - 1) % KT) + 1;
+    if (kb != 0) {
+        job = {p.dp_tiles + static_cast<int>(ta), kb, ke, JOB_PARTIAL, 0, 0};
+    } else {
+        const int last = sk_unit_of(p, (ta + 1) * KT - 1, U);
+        job = {p.dp_tiles + static_cast<int>(ta), 0, ke, JOB_FINISH, u + 1, last + 1};
+    }
+    return true;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Named barrier over the four epilogue warps (128 threads).
+__device__ __forceinline__ void epilogue_bar_sync() {
+    asm volatile("barrier.sync 1, 128;" ::: "memory");
 }
 
 __device__ __forceinline__ void store_row_chunk(const TcParams& p, int row, int col0,
@@ -304,12 +393,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            for (int t = unit; ok && t < p.num_tiles; t += num_units) {
+            Job job;
+            for (int j = 0; ok && next_job(p, unit, num_units, j, job); ++j) {
                 int tm, tn;
-                tile_coords(p, t, tm, tn);
+                tile_coords(p, job.tile, tm, tn);
                 const int a_row = tm * TILE_M + static_cast<int>(rank) * BM;
                 const int b_col = tn * p.bn + static_cast<int>(rank) * b_cols;
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = job.kb; kt < job.ke; ++kt) {
                     if (!bounded_wait<PAIR>(empty_bar(s), ph ^ 1u, abort_flag, p.wait_limit_ns,
                                             ROLE_PRODUCER, it, peer_rank)) {
                         ok = false;
@@ -387,7 +477,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int it = 0;
             int lt = 0;
             bool ok = true;
-            for (int t = unit; ok && t < p.num_tiles; t += num_units, ++lt) {
+            Job job;
+            for (int j = 0; ok && next_job(p, unit, num_units, j, job); ++j, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
                 if (!bounded_wait<PAIR>(tempty_bar(acc), acc_ph ^ 1u, abort_flag, p.wait_limit_ns,
@@ -397,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.bn);
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = job.kb; kt < job.ke; ++kt) {
                     if (!bounded_wait<PAIR>(full_bar(s), ph, abort_flag, p.wait_limit_ns, ROLE_MMA,
                                             it, peer_rank)) {
                         ok = false;
@@ -410,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = smem_desc(a_s + kk * 32u, 16u, 1024u);
                         const uint64_t bd = smem_desc(b_s + kk * b_kstep, b_lbo, 1024u);
-                        const uint32_t accum = (kt | kk) != 0 ? 1u : 0u;
+                        const uint32_t accum = (kt != job.kb || kk != 0) ? 1u : 0u;
                         if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
                         else umma_f16(d_tmem, ad, bd, p.idesc, accum);
                     }
@@ -439,29 +530,102 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = static_cast<int>(rank) * BM + 32 * q + lane;
+        const int row_in_cta = 32 * q + lane;
+        const int row_in_tile = static_cast<int>(rank) * BM + row_in_cta;
         const uint32_t tempty_leader0 = PAIR ? mapa_shared(tempty_bar(0), 0u) : tempty_bar(0);
+        const int ctas_per_unit = PAIR ? 2 : 1;
+        const size_t slot_floats = static_cast<size_t>(BM) * p.bn;  // one CTA's partial
+        volatile int* epi_ok = ctl->epi_ok;
         int lt = 0;
-        for (int t = unit; t < p.num_tiles; t += num_units, ++lt) {
+        Job job;
+        for (int j = 0; next_job(p, unit, num_units, j, job); ++j, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
-            if (!bounded_wait<PAIR>(tfull_bar(acc), acc_ph, abort_flag, p.wait_limit_ns,
-                                    ROLE_EPILOGUE, lt, peer_rank))
-                break;
+            // One thread waits (for the accumulator and, when finishing a
+            // stream-K tile, for the other segments' partials) and tells the
+            // other 127 through shared memory: every epilogue thread takes the
+            // same path, so the named barriers below always fill.
+            if (warp == 2 && lane == 0) {
+                bool ok = bounded_wait<PAIR>(tfull_bar(acc), acc_ph, abort_flag, p.wait_limit_ns,
+                                             ROLE_EPILOGUE, lt, peer_rank);
+                if (ok && job.role == JOB_FINISH) {
+                    for (int u2 = job.slot_lo; ok && u2 < job.slot_hi; ++u2) {
+                        const unsigned int* f = p.ws_flag + u2 * ctas_per_unit + rank;
+                        const unsigned long long t0 = globaltimer_ns();
+                        while (ld_acquire_gpu(f) == 0u) {
+                            if (*abort_flag) {
+                                ok = false;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+                                record_timeout(ROLE_EPILOGUE, lt);
+                                raise_abort<PAIR>(abort_flag, peer_rank);
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                }
+                epi_ok[j & 1] = ok ? 1 : 0;
+            }
+            __syncwarp();
+            epilogue_bar_sync();
+            if (!epi_ok[j & 1]) break;
+            if (job.role == JOB_FINISH) __threadfence();  // read the partials after the flags
             tc_fence_after();
             int tm, tn;
-            tile_coords(p, t, tm, tn);
+            tile_coords(p, job.tile, tm, tn);
             const int row = tm * TILE_M + row_in_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(acc * p.bn);
+            float* my_slot = p.ws + (static_cast<size_t>(unit) * ctas_per_unit + rank) * slot_floats +
+                             static_cast<size_t>(row_in_cta) * p.bn;
             for (int c = 0; c < p.bn; c += 16) {
                 uint32_t r[16];
                 tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
                 tmem_ld_wait();
+                if (job.role == JOB_PARTIAL) {
+                    // Publish this segment's fp32 partial (rows past M are
+                    // written too: the slot is private to this unit).
+                    float4* dst = reinterpret_cast<float4*>(my_slot + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                             __uint_as_float(r[4 * i + 2]),
+                                             __uint_as_float(r[4 * i + 3]));
+                    continue;
+                }
+                if (job.role == JOB_FINISH) {
+                    // acc(k from 0) + partial(unit lo) + ... in unit order.
+                    for (int u2 = job.slot_lo; u2 < job.slot_hi; ++u2) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            p.ws + (static_cast<size_t>(u2) * ctas_per_unit + rank) * slot_floats +
+                            static_cast<size_t>(row_in_cta) * p.bn + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 v = __ldcg(src + i);  // written by another SM: read L2
+                            r[4 * i + 0] = __float_as_uint(__uint_as_float(r[4 * i + 0]) + v.x);
+                            r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
+                            r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
+                            r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
+                        }
+                    }
+                }
                 const int col0 = tn * p.bn + c;
                 if (row < p.M && col0 < p.N) store_row_chunk(p, row, col0, r);
             }
             tc_fence_before();
+            if (job.role == JOB_PARTIAL) {
+                __threadfence();
+                epilogue_bar_sync();  // all 128 rows of this CTA's partial are written
+                if (warp == 2 && lane == 0)
+                    st_release_gpu(p.ws_flag + unit * ctas_per_unit + rank, 1u);
+            } else if (job.role == JOB_FINISH && job.slot_lo < job.slot_hi) {
+                epilogue_bar_sync();  // every row has read the partials: re-arm the flags
+                if (warp == 2 && lane == 0)
+                    for (int u2 = job.slot_lo; u2 < job.slot_hi; ++u2)
+                        p.ws_flag[u2 * ctas_per_unit + rank] = 0u;
+            }
             __syncwarp();
             if (lane == 0) {
                 if constexpr (PAIR) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
@@ -583,7 +747,38 @@ struct Geometry {
     int cluster = 1;   // CTAs per cluster
     size_t smem = 0;   // dynamic shared memory per CTA
     int units = 0;     // persistent workers (CTAs, or CTA pairs)
+    size_t ws_bytes = 0;  // stream-K workspace (partials + flags), 0 if unused
 };
+
+// Byte offset of the flags inside a workspace of `units` partial slots.
+size_t ws_flag_offset(int units, int ctas_per_unit, int bn) {
+    return static_cast<size_t>(units) * ctas_per_unit * BM * bn * sizeof(float);
+}
+
+// Stream-K workspaces, one per (device, stream): calls on one stream are
+// ordered, so they never share a workspace concurrently.
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int workspace_for(int dev, cudaStream_t stream, size_t bytes, size_t flag_off, void** out) {
+    std::lock_guard<std::mutex> g(g_ws_mu);
+    Workspace& w = g_ws[{dev, stream}];
+    if (w.bytes < bytes) {
+        if (w.ptr) cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMemset(w.ptr, 0, bytes) != cudaSuccess) return GEMM_ERR_CUDA;
+        w.bytes = bytes;
+    }
+    (void)flag_off;
+    *out = w.ptr;
+    return GEMM_OK;
+}
 
 // Parameters and launch geometry of one call (no launch).
 int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
@@ -618,6 +813,10 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.ldc = L.ldc;
     p.wait_limit_ns = static_cast<unsigned long long>(L.wait_limit_ns);
     p.withhold = L.withhold_arrive;
+    p.dp_tiles = p.num_tiles;
+    p.sk_iters = 0;
+    p.ws = nullptr;
+    p.ws_flag = nullptr;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -626,20 +825,38 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (!smem_attribute(dev, pair)) return GEMM_ERR_LAUNCH;
 
     size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) + sizeof(SharedCtl);
-    // A 256-wide tile uses all 512 TMEM columns: keep one CTA per SM.
-    if (bn == 256 && smem < 120 * 1024) smem = 120 * 1024;
+    // One CTA per SM: a 256-wide tile uses all 512 TMEM columns, and a
+    // stream-K finisher must never wait on a unit that is itself waiting for
+    // TMEM held by another CTA of the same SM.
+    if (smem < 120 * 1024) smem = 120 * 1024;
     geo.smem = smem;
-    if (!pair) {
-        geo.cluster = 1;
-        geo.units = p.num_tiles < sms ? p.num_tiles : sms;
-        geo.grid = geo.units;
-    } else {
-        const int max_pairs = max_resident_pairs(dev, smem);
-        if (max_pairs <= 0) return GEMM_ERR_LAUNCH;
-        geo.cluster = 2;
-        geo.units = p.num_tiles < max_pairs ? p.num_tiles : max_pairs;
-        geo.grid = 2 * geo.units;
+    int max_units = sms;
+    if (pair) {
+        max_units = max_resident_pairs(dev, smem);
+        if (max_units <= 0) return GEMM_ERR_LAUNCH;
     }
+    // Stream-K tail: when the last round of full tiles would leave units idle,
+    // cut the leftover tiles into K segments over all units (each unit's share
+    // is under one tile, so it touches at most two tiles).
+    const int T = p.num_tiles, KT = p.k_tiles, U = max_units;
+    const int rem = T % U;
+    const int sk_tiles = T < U ? T : rem;
+    // Automatic scheduling uses whole tiles: measured on GB300 the stream-K
+    // fix-up (a second epilogue per unit that publishes, then reduces its
+    // partial through the workspace) costs more than the idle tail it removes
+    // (8192^3: 1496 vs 1528 TFLOP/s; 2048^3: 340 vs 695).
+    const bool use_sk = L.schedule == 2 && rem != 0 && static_cast<long long>(sk_tiles) * KT >= U;
+    if (use_sk) {
+        p.dp_tiles = T - sk_tiles;
+        p.sk_iters = static_cast<long long>(sk_tiles) * KT;
+        geo.units = U;
+        const int cpu = pair ? 2 : 1;
+        geo.ws_bytes = ws_flag_offset(U, cpu, bn) + static_cast<size_t>(U) * cpu * sizeof(unsigned int);
+    } else {
+        geo.units = T < U ? T : U;
+    }
+    geo.cluster = pair ? 2 : 1;
+    geo.grid = geo.cluster * geo.units;
     return GEMM_OK;
 }
 
@@ -661,8 +878,18 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     }
     TcParams p;
     Geometry geo;
-    const int st = plan(L, p, geo);
+    int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
+    if (geo.ws_bytes) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+        void* ws = nullptr;
+        const size_t flag_off = ws_flag_offset(geo.units, pair ? 2 : 1, bn);
+        st = workspace_for(dev, stream, geo.ws_bytes, flag_off, &ws);
+        if (st != GEMM_OK) return st;
+        p.ws = static_cast<float*>(ws);
+        p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
+    }
     if (!pair) {
         gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, p);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
@@ -683,6 +910,18 @@ int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {
     if (grid) *grid = geo.grid;
     if (cluster) *cluster = geo.cluster;
     if (smem_bytes) *smem_bytes = static_cast<int>(geo.smem);
+    return GEMM_OK;
+}
+
+// After a run that gave up, a finisher may have left contributors' flags
+// set: clear the flags of every workspace of the current device.
+int tc_clear_workspace_flags() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> g(g_ws_mu);
+    for (auto& kv : g_ws)
+        if (kv.first.first == dev && kv.second.ptr)
+            if (cudaMemset(kv.second.ptr, 0, kv.second.bytes) != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
 

@@ -30,6 +30,7 @@ struct TcLaunch {
     int stages;       // 1..6
     int tile_n;       // tile width: 128 or 256
     int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256
+    int schedule;     // 0 auto, 1 full tiles only, 2 stream-K tail whenever a round is partial
     int64_t wait_limit_ns;
     int withhold_arrive;
 };
@@ -53,6 +54,9 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream);
 // Launch geometry tc_launch would use (CTAs, CTAs per cluster, dynamic
 // shared memory per CTA), without launching.
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes);
+// Zero the stream-K flags of every workspace of the current device (after a
+// run that gave up; synchronous).
+int tc_clear_workspace_flags();
 // Read the device status word of the tensor-core kernel on the current device
 // and reset it to zero (synchronous).
 int tc_read_and_clear_status(GemmDeviceStatus* out);

@@ -38,7 +38,7 @@ SIMT_FRAGMENTS_SINGLE = 1
 # Every extern "C" symbol include/gemm.h declares.
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
            "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
-           "pipelined_copy")
+           "pipelined_copy", "gemm_schedule_set")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p, p, p]
         lib.pipelined_copy.argtypes = [p, p, i64, i32, p]
         lib.pipelined_copy.restype = i32
+        lib.gemm_schedule_set.argtypes = [i32]
+        lib.gemm_schedule_set.restype = i32
         if path == LIB_PATH:
             _lib = lib
         return lib
@@ -225,6 +227,16 @@ def pipelined_copy(dst: torch.Tensor, src: torch.Tensor, stages: int = 2,
     if st != GEMM_OK:
         raise GemmError(st, "pipelined_copy")
     return dst
+
+
+SCHEDULE_AUTO, SCHEDULE_FULL_TILES, SCHEDULE_STREAM_K = 0, 1, 2
+
+
+def schedule_set(schedule: int) -> None:
+    """Tile schedule of the tensor-core kernel (libgemm.so gemm_schedule_set)."""
+    st = load_library().gemm_schedule_set(int(schedule))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_schedule_set")
 
 
 def debug_set(wait_limit_ns: int = 0, withhold_arrive: int = -1) -> None:

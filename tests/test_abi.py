@@ -185,3 +185,10 @@ def test_pipelined_copy_argument_checks(lib):
     assert c(P, P + 32, 64, 2, None) == G.GEMM_ERR_ARG       # overlapping ranges
     assert c(P + 8, P + 4096, 64, 2, None) == G.GEMM_ERR_ALIGN
     assert c(P, P + 4096, 40, 2, None) == G.GEMM_ERR_ALIGN   # not a multiple of 16
+
+
+def test_schedule_hook(lib):
+    assert lib.gemm_schedule_set(-1) == G.GEMM_ERR_ARG
+    assert lib.gemm_schedule_set(3) == G.GEMM_ERR_ARG
+    for v in (1, 2, 0):
+        assert lib.gemm_schedule_set(v) == G.GEMM_OK

@@ -308,3 +308,71 @@ def test_full_size_stage_sweep_is_bitwise_invariant():
                 base = C
             else:
                 assert torch.equal(C, base), f"tile={tile} stages={s}"
+
+
+# --------------------------------------------------------------------------- stream-K tail
+@pytest.fixture
+def stream_k():
+    G.schedule_set(G.SCHEDULE_STREAM_K)
+    yield
+    G.schedule_set(G.SCHEDULE_AUTO)
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("dtype", [GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32])
+@pytest.mark.parametrize("shape", [(768, 1280, 1024), (300, 520, 2000), (1100, 900, 4096)])
+def test_stream_k_matches_oracle(stream_k, tile, dtype, shape):
+    """Fewer tiles than persistent units: every tile is cut along K over
+    several units (up to ~5 contributors per tile) and reduced by the unit
+    that holds k = 0."""
+    M, N, K = shape
+    inp = make_inputs(workload(dtype, M, N, K, beta=0.0))
+    out, _ = run_gpu(inp, 4, tile=tile)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, dtype, what=f"stream-K {shape} tile={tile} dt={dtype}")
+
+
+@pytest.mark.parametrize("tile", TILES)
+def test_stream_k_stage_invariance_and_beta(stream_k, tile):
+    w = workload(GEMM_BF16_F32, 700, 1000, 1500, beta=1.0)
+    inp = make_inputs(w)
+    outs = {s: run_gpu(inp, s, tile=tile)[0] for s in TILE_STAGES[tile]}
+    base = outs[TILE_STAGES[tile][0]]
+    for s, o in outs.items():
+        assert np.array_equal(o, base), f"stream-K stages={s} differs (tile={tile})"
+    ref, absb = oracle_full(inp)
+    check_against_oracle(base, ref, absb, GEMM_BF16_F32, beta=1.0, C0=inp.C0,
+                         what=f"stream-K beta=1 tile={tile}")
+
+
+def test_stream_k_schedules_agree_within_tolerance():
+    inp = make_inputs(workload(GEMM_BF16_F32, 1024, 1536, 2048, beta=0.0))
+    ref, absb = oracle_full(inp)
+    outs = {}
+    try:
+        for sched in (G.SCHEDULE_FULL_TILES, G.SCHEDULE_STREAM_K, G.SCHEDULE_AUTO):
+            G.schedule_set(sched)
+            outs[sched], _ = run_gpu(inp, 4, tile=G.TILE_256x256_2SM)
+            check_against_oracle(outs[sched], ref, absb, GEMM_BF16_F32, what=f"schedule {sched}")
+    finally:
+        G.schedule_set(G.SCHEDULE_AUTO)
+
+
+@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM])
+def test_stream_k_timeout_leaves_context_usable(stream_k, tile):
+    inp = make_inputs(workload(GEMM_BF16_F32, 512, 768, 1024, beta=0.0))
+    A = to_device_padded(inp.A)
+    B = to_device_padded(inp.B)
+    C = torch.zeros(512, 768, device="cuda")
+    try:
+        # under stream-K block 0 may own a single K iteration: withhold the first
+        G.debug_set(50_000_000, 0)
+        with pytest.raises(G.GemmError) as e:
+            G.gemm(A, B, C, stages=2, tile=tile, checked=True)
+        assert e.value.status == G.GEMM_ERR_TIMEOUT
+    finally:
+        G.debug_set(0, -1)
+    G.gemm(A, B, C, stages=2, tile=tile, checked=True)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(C.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
+                         what="stream-K after timeout")
