@@ -99,7 +99,8 @@ typedef enum {
     GEMM_ERR_ALIGN = -3,        /* a 16-byte alignment rule above is broken */
     GEMM_ERR_LAUNCH = -4,       /* the CUDA launch (or tensor-map encode) failed */
     GEMM_ERR_TIMEOUT = -5,      /* a pipeline wait ran out (gemm_checked only) */
-    GEMM_ERR_CUDA = -6          /* another CUDA runtime call failed (copies, sync, device) */
+    GEMM_ERR_CUDA = -6,         /* another CUDA runtime call failed (copies, sync, device) */
+    GEMM_ERR_SCRATCH = -7       /* gemm_noalloc: needs more scratch than its fixed array */
 } gemm_status_t;
 
 /*
@@ -191,6 +192,40 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_
  * another value.
  */
 int gemm_schedule_set(int schedule);
+
+/*
+ * gemm_noalloc -- gemm_ex on the tensor-core path with the stream-K tail
+ * schedule (gemm_schedule_set's mode 2), for callers that must not allocate
+ * device memory.  (This entry point has no counterpart on the pages: it is a
+ * packaging of the same kernel.)
+ *
+ * Who needs it: code that cannot call cudaMalloc at the point where it runs
+ * the GEMM -- for example a caller whose device memory is all owned by its
+ * own pool or arena allocator, a latency-sensitive loop that must not hit the
+ * implicit device synchronisation of cudaMalloc/cudaFree, or a process that
+ * has handed out its free device memory.  gemm_ex's stream-K schedule
+ * allocates its workspace on first use; this entry point instead keeps the
+ * fp32 partial tiles and their flags in a fixed 20 MiB array inside the
+ * library's device image (held by every GPU that loads the library, until the
+ * process exits), and calls no allocating routine at all.
+ *
+ * Arguments, layout, alignment and return codes: as gemm_ex, tensor-core
+ * dtypes only (GEMM_F32 gives GEMM_ERR_UNSUPPORTED).  A launch whose
+ * workspace (one 128 x tile-width fp32 partial per CTA, plus flags; 19.9 MB
+ * for the default tile on 152 SMs) exceeds 20 MiB is refused with
+ * GEMM_ERR_SCRATCH before anything is enqueued.
+ *
+ * Every call shares the one array (per GPU).  Each call clears the flags it
+ * uses with cudaMemsetAsync on `stream` before its kernel (the array keeps
+ * the previous call's contents).  Calls that overlap on the GPU -- on
+ * different streams, or from different threads -- race on the array: order
+ * them on one stream.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) and sets the kernel's shared-memory
+ * limit; make that first call before any stream capture on that device.
+ */
+int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                 int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
+                 int b_col_major, int tile, void* stream);
 
 /*
  * pipelined_copy -- dst[0 .. n_bytes) = src[0 .. n_bytes), streamed through a

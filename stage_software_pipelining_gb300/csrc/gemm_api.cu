@@ -255,6 +255,8 @@ const char* gemm_status_string(int status) {
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch or tensor-map encode failed";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a pipeline wait ran out";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime call failed";
+        case GEMM_ERR_SCRATCH:
+            return "GEMM_ERR_SCRATCH: the launch needs more scratch than gemm_noalloc's fixed array";
         default: return "unknown gemm status";
     }
 }
@@ -309,6 +311,22 @@ int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void
         return GEMM_ERR_ARG;  // overlapping ranges
     if (!aligned16(dst) || !aligned16(src) || n_bytes % 16 != 0) return GEMM_ERR_ALIGN;
     return ssp::copy_launch(dst, src, n_bytes, stages, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                 int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
+                 int b_col_major, int tile, void* stream) {
+    Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile);
+    if (v.status != GEMM_OK) return v.status;
+    if (!is_tc(dtype)) return GEMM_ERR_UNSUPPORTED;  // the SIMT kernel has no scratch variant
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (K == 0 || alpha == 0.0f)
+        return ssp::scale_launch(M, N, C, ldc, dtype == GEMM_BF16_BF16, beta, s);
+    ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages,
+                                 b_col_major, v.tile);
+    L.schedule = 2;  // stream-K tail, its partials in the fixed array
+    return ssp::tc_launch_noalloc(L, s);
 }
 
 int gemm_schedule_set(int schedule) {

@@ -902,6 +902,75 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+// The stream-K workspace of gemm_noalloc: a fixed array in the library's own
+// device memory, so that launching needs no cudaMalloc.  Every GPU that loads
+// this module holds it until the process exits.  In host code the name is a
+// stand-in for the device array: the kernel receives the address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// Device address of g_noalloc_scratch on `dev` (which must be current),
+// looked up once per device.
+int noalloc_scratch_address(int dev, void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return GEMM_ERR_CUDA;
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return GEMM_OK;
+}
+}  // namespace
+
+int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
+    const bool pair = L.pair != 0;
+    const int bn = L.tile_n;
+    const int b_cols = pair ? bn / 2 : bn;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
+    if (L.b_col_major) {
+        if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
+    } else {
+        if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
+    }
+    TcParams p;
+    Geometry geo;
+    int st = plan(L, p, geo);
+    if (st != GEMM_OK) return st;
+    if (geo.ws_bytes) {
+        if (geo.ws_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+        void* ws = nullptr;
+        st = noalloc_scratch_address(dev, &ws);
+        if (st != GEMM_OK) return st;
+        const size_t flag_off = ws_flag_offset(geo.units, pair ? 2 : 1, bn);
+        // The array keeps the previous call's contents: the flags must start at 0.
+        if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + flag_off, 0, geo.ws_bytes - flag_off,
+                            stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        p.ws = static_cast<float*>(ws);
+        p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
+    }
+    if (!pair) {
+        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, p);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, p) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {
     TcParams p;
     Geometry geo;

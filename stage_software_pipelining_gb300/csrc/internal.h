@@ -51,6 +51,13 @@ struct SimtLaunch {
 // Enqueue the tensor-core GEMM (K > 0, M > 0, N > 0, alpha != 0).  Returns a
 // gemm_status_t.
 int tc_launch(const TcLaunch& L, cudaStream_t stream);
+// Size of the fixed stream-K workspace of gemm_noalloc (20 MiB: one 128 x 256
+// fp32 partial per CTA for 152 CTAs, plus flags).
+constexpr size_t kNoAllocScratchBytes = size_t(20) << 20;
+// tc_launch with the stream-K tail schedule and its workspace in that fixed
+// array: no allocation.  GEMM_ERR_SCRATCH if the launch needs more.
+int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream);
+
 // Launch geometry tc_launch would use (CTAs, CTAs per cluster, dynamic
 // shared memory per CTA), without launching.
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes);

@@ -24,6 +24,7 @@ GEMM_ERR_ALIGN = -3
 GEMM_ERR_LAUNCH = -4
 GEMM_ERR_TIMEOUT = -5
 GEMM_ERR_CUDA = -6
+GEMM_ERR_SCRATCH = -7
 
 # Tensor-core tiles (gemm_tile_t)
 TILE_AUTO = 0
@@ -38,7 +39,7 @@ SIMT_FRAGMENTS_SINGLE = 1
 # Every extern "C" symbol include/gemm.h declares.
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
            "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
-           "pipelined_copy", "gemm_schedule_set")
+           "pipelined_copy", "gemm_schedule_set", "gemm_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_ex.argtypes = base + [i32, i32, p]
         lib.gemm_checked.argtypes = base + [i32, i32, p]
         lib.gemm_host.argtypes = base + [i32, i32, p]
+        lib.gemm_noalloc.argtypes = base + [i32, i32, p]
+        lib.gemm_noalloc.restype = i32
         for name in ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
                      "gemm_max_stages", "gemm_plan", "gemm_debug_set"):
             getattr(lib, name).restype = i32

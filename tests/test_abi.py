@@ -123,7 +123,7 @@ def test_empty_output_is_a_noop(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         s = lib.gemm_status_string(code).decode()
         assert s.startswith("GEMM_")
     assert "unknown" in lib.gemm_status_string(42).decode()
@@ -192,3 +192,16 @@ def test_schedule_hook(lib):
     assert lib.gemm_schedule_set(3) == G.GEMM_ERR_ARG
     for v in (1, 2, 0):
         assert lib.gemm_schedule_set(v) == G.GEMM_OK
+
+
+def test_noalloc_entry_validates_on_the_host(lib):
+    na = lib.gemm_noalloc
+    # the same argument checks as gemm_ex, answered before any CUDA call
+    assert na(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0, None) == G.GEMM_ERR_ARG
+    assert na(8, 16, 24, P + 2, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+              None) == G.GEMM_ERR_ALIGN
+    # the SIMT path has no scratch, so no allocation-free variant
+    assert na(8, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_F32, 2, 0, 0,
+              None) == G.GEMM_ERR_UNSUPPORTED
+    assert na(0, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0, None) == G.GEMM_OK
+    assert "fixed array" in lib.gemm_status_string(G.GEMM_ERR_SCRATCH).decode()
