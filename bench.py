@@ -169,6 +169,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ----------------------------------------------------------------------------- ranks
+def rank_max(value: float, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); `value`
+    itself without a process group.  NCCL ranks pass their CUDA device, gloo
+    ranks the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank_step: float, steps: int, world: int, slowest_s: float) -> float:
+    """Units per second of the whole job: every rank does the same work per
+    step (weak scaling), the job ends with the slowest rank."""
+    return work_per_rank_step * steps * world / slowest_s
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -232,13 +252,9 @@ def run_ours(args):
     clocks = sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     launch_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = rank_max(elapsed_ms, dev)
     flops_step = w.flops
-    value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops_step, args.steps, world, elapsed_ms * 1e-3) / 1e12
 
     # the stage sweep (same workload, same launch stream)
     sweep = []
@@ -293,17 +309,13 @@ def run_ours(args):
         for _ in range(e2e_steps):
             G.gemm_host(hA, hB, hC, w.alpha, w.beta, stages=stages, tile=tile, stream=stream)
         barrier()
-        h_s = time.perf_counter() - h0
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([h_s], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            h_s = float(tt.item())
+        h_s = rank_max(time.perf_counter() - h0, dev)
         h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
         if w.beta != 0.0:
             h2d += hC.numel() * hC.element_size()
         d2h = hC.numel() * hC.element_size()
-        e2e = {"value": round(flops_step * e2e_steps * world / h_s / 1e12, 2), "unit": UNIT,
+        e2e = {"value": round(whole_job_rate(flops_step, e2e_steps, world, h_s) / 1e12, 2),
+               "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": e2e_steps, "entry": "gemm_host (pinned host buffers)"}
         G.load_library().gemm_host_release()

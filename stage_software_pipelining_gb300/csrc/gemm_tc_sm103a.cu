@@ -61,6 +61,7 @@ constexpr int UMMA_K = 16;              // K per tcgen05.mma (kind::f16)
 constexpr int NUM_THREADS = 192;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64 x 64 box, 8 KB
+constexpr int EPI_BYTES = 4 * 2 * 4096;      // epilogue staging: 4 warps x 2 boxes
 constexpr int ROLE_PRODUCER = 0, ROLE_MMA = 1, ROLE_EPILOGUE = 2;
 
 struct TcParams {
@@ -243,68 +244,45 @@ __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("barrier.sync 1, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ void store_row_chunk(const TcParams& p, int row, int col0,
-                                                const uint32_t (&r)[16]) {
-    float v[16];
+// Coalesced load of the C box a warp writes (32 rows x 128 bytes from
+// (row_base, col_base)): lane l loads 16 bytes of rows 4i + l/8, 16-byte
+// column l%8, for i = 0..7.  Elements outside M x N read as zero.
+__device__ __forceinline__ void load_c_box(const TcParams& p, int row_base, int col_base, int lane,
+                                           uint4 (&out)[8]) {
+    const int es = p.out_bf16 ? 2 : 4;
+    const int epc = 16 / es;  // elements per 16 bytes
+    const int col = col_base + (lane & 7) * epc;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = p.alpha * __uint_as_float(r[i]);
-    const bool full = col0 + 16 <= p.N;
-    if (p.out_bf16) {
-        __nv_bfloat16* c = static_cast<__nv_bfloat16*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
-        if (p.beta != 0.0f) {
-            if (full) {
-                uint4 u[2];
-                u[0] = *reinterpret_cast<const uint4*>(c);
-                u[1] = *reinterpret_cast<const uint4*>(c + 8);
-                const __nv_bfloat16* cb = reinterpret_cast<const __nv_bfloat16*>(u);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = fmaf(p.beta, __bfloat162float(cb[i]), v[i]);
+    for (int i = 0; i < 8; ++i) {
+        const int row = row_base + 4 * i + (lane >> 3);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < p.M && col < p.N) {
+            const char* base = static_cast<const char*>(p.C) +
+                               (static_cast<long long>(row) * p.ldc + col) * es;
+            if (col + epc <= p.N) {
+                v = *reinterpret_cast<const uint4*>(base);
+            } else if (es == 4) {  // ragged N edge: only the columns below N
+                const uint32_t* b32 = reinterpret_cast<const uint32_t*>(base);
+                v.x = b32[0];
+                v.y = col + 1 < p.N ? b32[1] : 0u;
+                v.z = col + 2 < p.N ? b32[2] : 0u;
+                v.w = col + 3 < p.N ? b32[3] : 0u;
             } else {
+                const uint16_t* b16 = reinterpret_cast<const uint16_t*>(base);
+                uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (col0 + i < p.N) v[i] = fmaf(p.beta, __bfloat162float(c[i]), v[i]);
-            }
-        }
-        if (full) {
-            uint4 u[2];
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(u);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            *reinterpret_cast<uint4*>(c) = u[0];
-            *reinterpret_cast<uint4*>(c + 8) = u[1];
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (col0 + i < p.N) c[i] = __float2bfloat16_rn(v[i]);
-        }
-    } else {
-        float* c = static_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col0;
-        if (p.beta != 0.0f) {
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 o = *reinterpret_cast<const float4*>(c + 4 * q);
-                    v[4 * q + 0] = fmaf(p.beta, o.x, v[4 * q + 0]);
-                    v[4 * q + 1] = fmaf(p.beta, o.y, v[4 * q + 1]);
-                    v[4 * q + 2] = fmaf(p.beta, o.z, v[4 * q + 2]);
-                    v[4 * q + 3] = fmaf(p.beta, o.w, v[4 * q + 3]);
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t h = col + e < p.N ? static_cast<uint32_t>(b16[e]) : 0u;
+                    const uint32_t sh = (e & 1) * 16u;
+                    if (e < 2) w0 |= h << sh;
+                    else if (e < 4) w1 |= h << sh;
+                    else if (e < 6) w2 |= h << sh;
+                    else w3 |= h << sh;
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (col0 + i < p.N) v[i] = fmaf(p.beta, c[i], v[i]);
+                v = make_uint4(w0, w1, w2, w3);
             }
         }
-        if (full) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<float4*>(c + 4 * q) =
-                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (col0 + i < p.N) c[i] = v[i];
-        }
+        out[i] = v;
     }
 }
 
@@ -321,7 +299,7 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, int row, int 
 template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Swizzled TMA destinations and UMMA operands want 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -332,7 +310,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int b_stage_bytes = b_cols * BK * 2;
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * A_STAGE_BYTES;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(b_ring + S * b_stage_bytes);
+    uint8_t* epi_ring = b_ring + S * b_stage_bytes;  // 4 warps x 2 output boxes of 4 KB
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(epi_ring + EPI_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -531,11 +510,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_cta = 32 * q + lane;
-        const int row_in_tile = static_cast<int>(rank) * BM + row_in_cta;
         const uint32_t tempty_leader0 = PAIR ? mapa_shared(tempty_bar(0), 0u) : tempty_bar(0);
         const int ctas_per_unit = PAIR ? 2 : 1;
         const size_t slot_floats = static_cast<size_t>(BM) * p.bn;  // one CTA's partial
         volatile int* epi_ok = ctl->epi_ok;
+        // Output boxes of 32 rows x 128 bytes: 32 fp32 or 64 bf16 columns.
+        const int cw = p.out_bf16 ? 64 : 32;
+        const uint32_t epi_buf0 = smem_addr(epi_ring);
+        int chunk_seq = 0;
         int lt = 0;
         Job job;
         for (int j = 0; next_job(p, unit, num_units, j, job); ++j, ++lt) {
@@ -575,24 +557,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             int tm, tn;
             tile_coords(p, job.tile, tm, tn);
-            const int row = tm * TILE_M + row_in_tile;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(acc * p.bn);
-            float* my_slot = p.ws + (static_cast<size_t>(unit) * ctas_per_unit + rank) * slot_floats +
-                             static_cast<size_t>(row_in_cta) * p.bn;
-            for (int c = 0; c < p.bn; c += 16) {
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(t_row + static_cast<uint32_t>(c), r);
-                tmem_ld_wait();
-                if (job.role == JOB_PARTIAL) {
-                    // Publish this segment's fp32 partial (rows past M are
-                    // written too: the slot is private to this unit).
-                    float4* dst = reinterpret_cast<float4*>(my_slot + c);
+            const int row_base = tm * TILE_M + static_cast<int>(rank) * BM + 32 * q;  // this warp's rows
+            const size_t my_slot_off = (static_cast<size_t>(unit) * ctas_per_unit + rank) * slot_floats;
+            const int nchunks = p.bn / cw;
+            uint4 c_next[8];
+            if (p.beta != 0.0f && job.role != JOB_PARTIAL)
+                load_c_box(p, row_base, tn * p.bn, lane, c_next);
+            for (int ci = 0; ci < nchunks; ++ci, ++chunk_seq) {
+                const int c = ci * cw;
+                const int col_base = tn * p.bn + c;
+                const uint32_t buf = epi_buf0 + static_cast<uint32_t>(q) * 8192u +
+                                     static_cast<uint32_t>(chunk_seq & 1) * 4096u;
+                // The store that last used this buffer has read it.
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                uint4 c_cur[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                             __uint_as_float(r[4 * i + 2]),
-                                             __uint_as_float(r[4 * i + 3]));
+                for (int i = 0; i < 8; ++i) c_cur[i] = c_next[i];
+                if (p.beta != 0.0f && job.role != JOB_PARTIAL && ci + 1 < nchunks)
+                    load_c_box(p, row_base, col_base + cw, lane, c_next);  // in flight meanwhile
+                float f[64];
+                {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+                    if (cw == 64) {
+                        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c + 32), r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[32 + i] = __uint_as_float(r[i]);
+                    }
+                }
+                if (job.role == JOB_PARTIAL) {
+                    // Publish this segment's fp32 partial (rows past M too: the
+                    // slot is private to this unit).
+                    float4* dst = reinterpret_cast<float4*>(p.ws + my_slot_off +
+                                                            static_cast<size_t>(row_in_cta) * p.bn + c);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < cw / 4) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
                     continue;
                 }
                 if (job.role == JOB_FINISH) {
@@ -602,17 +609,92 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             p.ws + (static_cast<size_t>(u2) * ctas_per_unit + rank) * slot_floats +
                             static_cast<size_t>(row_in_cta) * p.bn + c);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float4 v = __ldcg(src + i);  // written by another SM: read L2
-                            r[4 * i + 0] = __float_as_uint(__uint_as_float(r[4 * i + 0]) + v.x);
-                            r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
-                            r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
-                            r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
+                        for (int i = 0; i < 16; ++i) {
+                            if (i < cw / 4) {
+                                const float4 v = __ldcg(src + i);  // written by another SM: read L2
+                                f[4 * i + 0] += v.x;
+                                f[4 * i + 1] += v.y;
+                                f[4 * i + 2] += v.z;
+                                f[4 * i + 3] += v.w;
+                            }
                         }
                     }
                 }
-                const int col0 = tn * p.bn + c;
-                if (row < p.M && col0 < p.N) store_row_chunk(p, row, col0, r);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) f[i] *= p.alpha;
+                if (p.beta != 0.0f) {
+                    // Stage the coalesced C box in the buffer, then read this
+                    // thread's row back: out = alpha*acc + beta*C.
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3), j = lane & 7;
+                        st_shared_v4(buf + rr * 128 + ((j ^ (rr & 7)) << 4), c_cur[i]);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 u = ld_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4));
+                        if (cw == 32) {
+                            f[4 * j + 0] = fmaf(p.beta, __uint_as_float(u.x), f[4 * j + 0]);
+                            f[4 * j + 1] = fmaf(p.beta, __uint_as_float(u.y), f[4 * j + 1]);
+                            f[4 * j + 2] = fmaf(p.beta, __uint_as_float(u.z), f[4 * j + 2]);
+                            f[4 * j + 3] = fmaf(p.beta, __uint_as_float(u.w), f[4 * j + 3]);
+                        } else {
+                            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 fc = __bfloat1622float2(h[e]);
+                                f[8 * j + 2 * e] = fmaf(p.beta, fc.x, f[8 * j + 2 * e]);
+                                f[8 * j + 2 * e + 1] = fmaf(p.beta, fc.y, f[8 * j + 2 * e + 1]);
+                            }
+                        }
+                    }
+                }
+                if (col_base + cw > p.N) {
+                    // A box across the N edge: the tensor store clips columns
+                    // only at 16-byte granularity, so each thread writes its
+                    // row's columns below N itself.
+                    const int row = row_base + lane;
+                    if (row < p.M) {
+                        if (p.out_bf16) {
+                            __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(p.C) +
+                                                static_cast<long long>(row) * p.ldc + col_base;
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < cw && col_base + i < p.N) cp[i] = __float2bfloat16_rn(f[i]);
+                        } else {
+                            float* cp = static_cast<float*>(p.C) +
+                                        static_cast<long long>(row) * p.ldc + col_base;
+#pragma unroll
+                            for (int i = 0; i < 64; ++i)
+                                if (i < cw && col_base + i < p.N) cp[i] = f[i];
+                        }
+                    }
+                    continue;
+                }
+                // This thread's row of the box, 128-byte swizzled as the tensor
+                // store expects, then one lane stores the 32-row box.
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 u;
+                    if (cw == 32) {
+                        u = make_uint4(__float_as_uint(f[4 * j]), __float_as_uint(f[4 * j + 1]),
+                                       __float_as_uint(f[4 * j + 2]), __float_as_uint(f[4 * j + 3]));
+                    } else {
+                        __nv_bfloat162 h[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            h[e] = __floats2bfloat162_rn(f[8 * j + 2 * e], f[8 * j + 2 * e + 1]);
+                        u = *reinterpret_cast<const uint4*>(h);
+                    }
+                    st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), u);
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0 && row_base < p.M && col_base < p.N) {  // boxes past M or N: nothing to store
+                    tma_store_2d(&tmC, buf, col_base, row_base);
+                    bulk_commit_group();
+                }
             }
             tc_fence_before();
             if (job.role == JOB_PARTIAL) {
@@ -634,6 +716,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_group_all();  // this warp's C stores are done
     __syncthreads();
     if constexpr (PAIR) cluster_sync_all();  // no remote arrive or multicast is still pending
     if (warp == 1) {
@@ -673,6 +756,24 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
                     2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Tensor map over C (rows x cols, leading dimension ld elements) for the
+// epilogue's box stores: 32 rows x 128 bytes (32 fp32 or 64 bf16 columns),
+// 128-byte swizzle.
+bool encode_c(CUtensorMap* map, void* base, bool bf16, uint64_t rows, uint64_t cols, uint64_t ld) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * es};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -824,7 +925,8 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (sms <= 0) return GEMM_ERR_CUDA;
     if (!smem_attribute(dev, pair)) return GEMM_ERR_LAUNCH;
 
-    size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) + sizeof(SharedCtl);
+    size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) + EPI_BYTES +
+                  sizeof(SharedCtl);
     // One CTA per SM: a 256-wide tile uses all 512 TMEM columns, and a
     // stream-K finisher must never wait on a unit that is itself waiting for
     // TMEM held by another CTA of the same SM.
@@ -866,7 +968,8 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
     const int bn = L.tile_n;
     const int b_cols = pair ? bn / 2 : bn;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_c(&tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return GEMM_ERR_LAUNCH;
     // A: M x K row-major, boxes of 64 (K) x 128 (M).
     if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
     if (L.b_col_major) {
@@ -891,13 +994,13 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
     }
     if (!pair) {
-        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, p);
+        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, tmC, p);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, tmC, p) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
@@ -933,7 +1036,8 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
     const int bn = L.tile_n;
     const int b_cols = pair ? bn / 2 : bn;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_c(&tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return GEMM_ERR_LAUNCH;
     if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
     if (L.b_col_major) {
         if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
@@ -960,13 +1064,13 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
     }
     if (!pair) {
-        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, p);
+        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, tmC, p);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, tmC, p) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
