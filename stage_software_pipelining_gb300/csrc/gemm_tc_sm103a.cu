@@ -71,6 +71,7 @@ struct TcParams {
     int stages;
     int bn;           // tile width (columns of C per tile)
     int b_mn_major;
+    int b_chunked;    // row-major B through a 3-D map: one copy per stage for all 64-column chunks
     int out_bf16;
     uint32_t idesc;
     float alpha, beta;
@@ -391,7 +392,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (PAIR && !leader) {
                             const uint32_t bar = leader_full0 + 8u * s;
                             tma_load_2d_pair(a_dst, &tmA, bar, kt * BK, a_row);
-                            if (p.b_mn_major) {
+                            if (p.b_chunked) {
+                                tma_load_3d_pair(b_dst, &tmB, bar, 0, kt * BK, b_col / 64);
+                            } else if (p.b_mn_major) {
                                 for (int j = 0; j < b_cols / 64; ++j)
                                     tma_load_2d_pair(b_dst + j * B_BOX_BYTES, &tmB, bar,
                                                      b_col + 64 * j, kt * BK);
@@ -400,7 +403,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         } else {
                             tma_load_2d(a_dst, &tmA, full_bar(s), kt * BK, a_row);
-                            if (p.b_mn_major) {
+                            if (p.b_chunked) {
+                                tma_load_3d(b_dst, &tmB, full_bar(s), 0, kt * BK, b_col / 64);
+                            } else if (p.b_mn_major) {
                                 for (int j = 0; j < b_cols / 64; ++j)
                                     tma_load_2d(b_dst + j * B_BOX_BYTES, &tmB, full_bar(s),
                                                 b_col + 64 * j, kt * BK);
@@ -759,6 +764,26 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+// Row-major B (K x N, N a multiple of 64) as a 3-D tensor: 64 columns
+// (contiguous), K rows (stride ld elements), N/64 chunks (stride 64 elements).
+// A box (64, BK, chunks) then lands chunk after chunk, each chunk's BK rows
+// of 128 bytes contiguous and 128-byte swizzled: the MN-major operand layout
+// the MMA reads, filled by one copy instead of one per chunk.
+bool encode_b_chunked(CUtensorMap* map, const void* base, bool bf16, uint64_t K, uint64_t N,
+                      uint64_t ld, uint32_t chunks) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, K, N / 64};
+    cuuint64_t strides[2] = {ld * 2, 128};
+    cuuint32_t box[3] = {64, BK, chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Tensor map over C (rows x cols, leading dimension ld elements) for the
 // epilogue's box stores: 32 rows x 128 bytes (32 fp32 or 64 bf16 columns),
 // 128-byte swizzle.
@@ -899,6 +924,7 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.stages = S;
     p.bn = bn;
     p.b_mn_major = L.b_col_major ? 0 : 1;
+    p.b_chunked = 0;
     p.out_bf16 = L.out_bf16;
     // Instruction descriptor (kind::f16): D fp32 (bit 4), A and B type
     // (bits 7..9, 10..12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B major
@@ -972,9 +998,14 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     if (!encode_c(&tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return GEMM_ERR_LAUNCH;
     // A: M x K row-major, boxes of 64 (K) x 128 (M).
     if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
+    const bool b_chunked = !L.b_col_major && L.N % 64 == 0;
     if (L.b_col_major) {
         // B column-major = N x K row-major: boxes of 64 (K) x b_cols (N).
         if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
+    } else if (b_chunked) {
+        // B row-major, N a multiple of 64: one 3-D box of b_cols/64 chunks per stage.
+        if (!encode_b_chunked(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, b_cols / 64))
+            return GEMM_ERR_LAUNCH;
     } else {
         // B row-major K x N: boxes of 64 (N) x 64 (K); b_cols/64 boxes per stage.
         if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
@@ -983,6 +1014,7 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     Geometry geo;
     int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
+    p.b_chunked = b_chunked ? 1 : 0;
     if (geo.ws_bytes) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
