@@ -96,8 +96,9 @@ TILE_NAMES = {128: "128x128x64 (1 SM)", 256: "128x256x64 (1 SM)",
               512: "256x256x64 (CTA pair, cta_group::2)"}
 TILE_MAX_STAGES = {128: 6, 256: 4, 512: 6}
 # Default ring depth per tile: the deepest ring that fits, except on the CTA
-# pair where 4 stages measured as fast as 6 (the copy latency is covered).
-TILE_DEFAULT_STAGES = {128: 6, 256: 4, 512: 4}
+# pair, where 5 stages measured fastest in long power-capped runs (4: 1490,
+# 5: 1519, 6: below 5 TFLOP/s).
+TILE_DEFAULT_STAGES = {128: 6, 256: 4, 512: 5}
 
 
 def committed_traffic(workload: str, stages: int, tile: int):

@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // The leader's full[s] counts the bytes of both CTAs of a pair.
             const uint32_t armed_bytes = PAIR ? 2u * stage_bytes : stage_bytes;
             const uint32_t leader_full0 = PAIR ? mapa_shared(full_bar(0), 0u) : full_bar(0);
+            // A panels are reused by the next round of tiles (tiles are walked
+            // in groups of tile rows): ask L2 to keep them over B and C lines.
+            const uint64_t a_policy = l2_policy_evict_last();
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (leader) mbar_arrive_expect_tx(full_bar(s), armed_bytes);
                         if (PAIR && !leader) {
                             const uint32_t bar = leader_full0 + 8u * s;
-                            tma_load_2d_pair(a_dst, &tmA, bar, kt * BK, a_row);
+                            tma_load_2d_pair_hint(a_dst, &tmA, bar, kt * BK, a_row, a_policy);
                             if (p.b_chunked) {
                                 tma_load_3d_pair(b_dst, &tmB, bar, 0, kt * BK, b_col / 64);
                             } else if (p.b_mn_major) {
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 tma_load_2d_pair(b_dst, &tmB, bar, kt * BK, b_col);
                             }
                         } else {
-                            tma_load_2d(a_dst, &tmA, full_bar(s), kt * BK, a_row);
+                            tma_load_2d_hint(a_dst, &tmA, full_bar(s), kt * BK, a_row, a_policy);
                             if (p.b_chunked) {
                                 tma_load_3d(b_dst, &tmB, full_bar(s), 0, kt * BK, b_col / 64);
                             } else if (p.b_mn_major) {

@@ -265,8 +265,10 @@ def sample_indices(M, N, count, seed):
     ("fp32_2048", 2, 0),
     ("fp16_2048", 4, 0),
     ("bf16_8192_beta1", 4, G.TILE_128x256),
+    ("bf16_8192_beta1", 5, G.TILE_256x256_2SM),     # the configuration bench.py times
     ("bf16_8192_beta1", 6, G.TILE_256x256_2SM),
     ("bf16_ragged_colB", 4, G.TILE_128x256),
+    ("bf16_ragged_colB", 5, G.TILE_256x256_2SM),
     ("bf16_ragged_colB", 6, G.TILE_256x256_2SM),
 ])
 def test_full_size_workload_sampled(name, stages, tile):
