@@ -153,7 +153,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
               int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
               int b_col_major, int tile, void* stream);
 
-/* Frees gemm_host's cached device buffers on the current device. */
+/* Frees the device buffers the library caches on the current device:
+ * gemm_host's staging buffers and the stream-K workspaces (gemm_schedule_set
+ * mode 2).  Call it when no GEMM of this library is running on the device;
+ * later calls allocate again as needed. */
 int gemm_host_release(void);
 
 /* Human-readable name of a gemm_status_t (static storage). */

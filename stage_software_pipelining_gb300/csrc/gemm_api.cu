@@ -236,14 +236,16 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
 int gemm_host_release(void) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
-    std::lock_guard<std::mutex> g(g_staging_mu);
-    Staging& s = g_staging[dev];
-    for (int i = 0; i < 3; ++i) {
-        if (s.ptr[i]) cudaFree(s.ptr[i]);
-        s.ptr[i] = nullptr;
-        s.cap[i] = 0;
+    {
+        std::lock_guard<std::mutex> g(g_staging_mu);
+        Staging& s = g_staging[dev];
+        for (int i = 0; i < 3; ++i) {
+            if (s.ptr[i]) cudaFree(s.ptr[i]);
+            s.ptr[i] = nullptr;
+            s.cap[i] = 0;
+        }
     }
-    return GEMM_OK;
+    return ssp::tc_release_workspaces();
 }
 
 const char* gemm_status_string(int status) {

@@ -1121,6 +1121,23 @@ int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {
     return GEMM_OK;
 }
 
+// Free the stream-K workspaces of the current device (the caller makes sure
+// no launch that uses them is still running).
+int tc_release_workspaces() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> g(g_ws_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == dev) {
+            if (it->second.ptr) cudaFree(it->second.ptr);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return GEMM_OK;
+}
+
 // After a run that gave up, a finisher may have left contributors' flags
 // set: clear the flags of every workspace of the current device.
 int tc_clear_workspace_flags() {

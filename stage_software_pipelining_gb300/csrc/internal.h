@@ -61,6 +61,8 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream);
 // Launch geometry tc_launch would use (CTAs, CTAs per cluster, dynamic
 // shared memory per CTA), without launching.
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes);
+// Free the stream-K workspaces of the current device.
+int tc_release_workspaces();
 // Zero the stream-K flags of every workspace of the current device (after a
 // run that gave up; synchronous).
 int tc_clear_workspace_flags();

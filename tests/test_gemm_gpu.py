@@ -378,3 +378,31 @@ def test_stream_k_timeout_leaves_context_usable(stream_k, tile):
     ref, absb = oracle_full(inp)
     check_against_oracle(C.double().cpu().numpy(), ref, absb, GEMM_BF16_F32,
                          what="stream-K after timeout")
+
+
+# --------------------------------------------------------------------------- streams
+def test_launch_goes_on_the_callers_stream():
+    """gemm enqueues on the stream it is given: work queued before it on that
+    stream is finished first, and an event recorded after it completes after."""
+    w = workload(GEMM_BF16_F32, 512, 512, 512, beta=1.0)
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    s = torch.cuda.Stream()
+    C = torch.empty(512, 512, device="cuda")
+    with torch.cuda.stream(s):
+        C.copy_(inp.C0.cuda(non_blocking=False))   # queued on s before the GEMM
+        G.gemm(A, B, C, 1.0, 1.0, stages=3, tile=G.TILE_256x256_2SM, stream=s)
+        done = torch.cuda.Event()
+        done.record(s)
+    done.synchronize()
+    ref, absb = oracle_full(inp)
+    check_against_oracle(C.double().cpu().numpy(), ref, absb, GEMM_BF16_F32, beta=1.0,
+                         C0=inp.C0, what="non-default stream")
+
+
+def test_release_then_reuse():
+    G.load_library().gemm_host_release()
+    inp = make_inputs(workload(GEMM_BF16_F32, 256, 256, 256, beta=0.0))
+    out, _ = run_gpu(inp, 2)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(out, ref, absb, GEMM_BF16_F32, what="after release")
