@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--tile", type=int, default=0,
                     help="tensor-core tile code: 0 auto, 128 (128x128), 256 (128x256), "
                          "512 (256x256 on a CTA pair)")
+    ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
+                    help="tensor-core tile schedule: 0 the library's automatic choice, "
+                         "1 whole tiles, 2 stream-K tail")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -95,6 +98,7 @@ def kernel_hash() -> str:
 TILE_NAMES = {128: "128x128x64 (1 SM)", 256: "128x256x64 (1 SM)",
               512: "256x256x64 (CTA pair, cta_group::2)"}
 TILE_MAX_STAGES = {128: 6, 256: 4, 512: 6}
+SCHEDULE_NAMES = {0: "automatic", 1: "whole tiles", 2: "stream-K tail"}
 # Default ring depth per tile: the deepest ring that fits, except on the CTA
 # pair, where 5 stages measured fastest in long power-capped runs (4: 1490,
 # 5: 1519, 6: below 5 TFLOP/s).
@@ -204,6 +208,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     G.load_library()
+    G.schedule_set(args.schedule)
 
     w = BY_NAME[args.workload]
     tile = args.tile
@@ -352,6 +357,7 @@ def run_ours(args):
             "data": "synthetic (seeded)",
             "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
                        "alpha": w.alpha, "beta": w.beta, "stages": stages,
+                       "schedule": SCHEDULE_NAMES[args.schedule],
                        "tile": "128x64x16 (SIMT)" if w.dtype == GEMM_F32
                        else TILE_NAMES[tile], "b_layout": "col" if w.b_col_major else "row",
                        "l2": f"inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.0f} MB "

@@ -61,7 +61,9 @@ constexpr int UMMA_K = 16;              // K per tcgen05.mma (kind::f16)
 constexpr int NUM_THREADS = 192;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64 x 64 box, 8 KB
-constexpr int EPI_BYTES = 4 * 2 * 4096;      // epilogue staging: 4 warps x 2 boxes
+constexpr int EPI_BOX_BYTES = 4096;         // one output box: 32 rows x 128 bytes
+constexpr int kEpiMaxBufs = 4;              // output boxes per epilogue warp, at most
+constexpr int kTcMaxSmem = 227 * 1024;      // dynamic shared memory a CTA may opt in to
 constexpr int ROLE_PRODUCER = 0, ROLE_MMA = 1, ROLE_EPILOGUE = 2;
 
 struct TcParams {
@@ -83,6 +85,7 @@ struct TcParams {
     // spread evenly over the persistent units (sk_iters = their k-tiles).
     int dp_tiles;
     long long sk_iters;
+    int epi_bufs;           // output boxes per epilogue warp (2..kEpiMaxBufs)
     float* ws;              // one partial tile per unit (per CTA: 128 x bn fp32)
     unsigned int* ws_flag;  // per unit and CTA rank: 1 = partial published
 };
@@ -101,6 +104,7 @@ struct Job {
 struct SharedCtl {
     // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
     unsigned long long bar[2 * kTcMaxStages128 + 5];
+    unsigned long long cbar[4 * kEpiMaxBufs];  // C box copies, per epilogue warp and box
     uint32_t tmem_base;
     int abort;
     int epi_ok[2];  // the epilogue's per-job go/abort decision, by job parity
@@ -245,48 +249,6 @@ __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("barrier.sync 1, 128;" ::: "memory");
 }
 
-// Coalesced load of the C box a warp writes (32 rows x 128 bytes from
-// (row_base, col_base)): lane l loads 16 bytes of rows 4i + l/8, 16-byte
-// column l%8, for i = 0..7.  Elements outside M x N read as zero.
-__device__ __forceinline__ void load_c_box(const TcParams& p, int row_base, int col_base, int lane,
-                                           uint4 (&out)[8]) {
-    const int es = p.out_bf16 ? 2 : 4;
-    const int epc = 16 / es;  // elements per 16 bytes
-    const int col = col_base + (lane & 7) * epc;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = row_base + 4 * i + (lane >> 3);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < p.M && col < p.N) {
-            const char* base = static_cast<const char*>(p.C) +
-                               (static_cast<long long>(row) * p.ldc + col) * es;
-            if (col + epc <= p.N) {
-                v = *reinterpret_cast<const uint4*>(base);
-            } else if (es == 4) {  // ragged N edge: only the columns below N
-                const uint32_t* b32 = reinterpret_cast<const uint32_t*>(base);
-                v.x = b32[0];
-                v.y = col + 1 < p.N ? b32[1] : 0u;
-                v.z = col + 2 < p.N ? b32[2] : 0u;
-                v.w = col + 3 < p.N ? b32[3] : 0u;
-            } else {
-                const uint16_t* b16 = reinterpret_cast<const uint16_t*>(base);
-                uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t h = col + e < p.N ? static_cast<uint32_t>(b16[e]) : 0u;
-                    const uint32_t sh = (e & 1) * 16u;
-                    if (e < 2) w0 |= h << sh;
-                    else if (e < 4) w1 |= h << sh;
-                    else if (e < 6) w2 |= h << sh;
-                    else w3 |= h << sh;
-                }
-                v = make_uint4(w0, w1, w2, w3);
-            }
-        }
-        out[i] = v;
-    }
-}
-
 // PAIR = false: one CTA computes a 128 x bn tile with tcgen05.mma.cta_group::1.
 // PAIR = true: a cluster of two CTAs computes a 256 x bn tile with
 // tcgen05.mma.cta_group::2: CTA rank r stages rows 128r..128r+127 of the A
@@ -311,8 +273,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int b_stage_bytes = b_cols * BK * 2;
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * A_STAGE_BYTES;
-    uint8_t* epi_ring = b_ring + S * b_stage_bytes;  // 4 warps x 2 output boxes of 4 KB
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(epi_ring + EPI_BYTES);
+    uint8_t* epi_ring = b_ring + S * b_stage_bytes;  // 4 warps x epi_bufs output boxes
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(epi_ring + 4 * p.epi_bufs * EPI_BOX_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -342,6 +304,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrive per epilogue warp (both CTAs)
         }
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < 4 * kEpiMaxBufs; ++b) mbar_init(smem_addr(&ctl->cbar[b]), 1);
         ctl->abort = 0;
         fence_barrier_init();
     }
@@ -517,20 +480,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_cta = 32 * q + lane;
         const uint32_t tempty_leader0 = PAIR ? mapa_shared(tempty_bar(0), 0u) : tempty_bar(0);
         const int ctas_per_unit = PAIR ? 2 : 1;
         const size_t slot_floats = static_cast<size_t>(BM) * p.bn;  // one CTA's partial
         volatile int* epi_ok = ctl->epi_ok;
         // Output boxes of 32 rows x 128 bytes: 32 fp32 or 64 bf16 columns.
         const int cw = p.out_bf16 ? 64 : 32;
-        const uint32_t epi_buf0 = smem_addr(epi_ring);
-        int chunk_seq = 0;
+        // This warp's ring of nb output boxes (32 rows x 128 bytes, 4 KB):
+        // with beta != 0 each box is first filled with C by a tensor copy
+        // (issued up to nb boxes ahead, the first ones before the accumulator
+        // is ready), updated in place, then stored by a tensor copy.
+        const int nb = p.epi_bufs;
+        const uint32_t epi_buf0 = smem_addr(epi_ring) + static_cast<uint32_t>(q * nb) * 4096u;
+        const uint32_t cbar0 = smem_addr(&ctl->cbar[q * kEpiMaxBufs]);
+        const bool load_c = p.beta != 0.0f;
+        uint32_t c_phase = 0;    // bit b: parity of the next C copy into box b
+        uint32_t c_pending = 0;  // bit b: a C copy into box b is issued and not yet consumed
         int lt = 0;
         Job job;
         for (int j = 0; next_job(p, unit, num_units, j, job); ++j, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
+            int tm, tn;
+            tile_coords(p, job.tile, tm, tn);
+            const int row_base = tm * TILE_M + static_cast<int>(rank) * BM + 32 * q;  // this warp's rows
+            const int col0 = tn * p.bn;
+            const int nchunks = p.bn / cw;
+            // A box goes through the tensor copies when it lies inside M x N
+            // but for rows past M (the copies fill and clip whole rows); a box
+            // across the N edge is read and written by each thread for its row.
+            auto tma_box = [&](int ci) {
+                return row_base < p.M && col0 + (ci + 1) * cw <= p.N;
+            };
+            auto issue_c = [&](int ci) {  // lane 0: copy C box ci into box ci % nb
+                const int b = ci % nb;
+                mbar_arrive_expect_tx(cbar0 + 8u * b, 4096u);
+                tma_load_2d(epi_buf0 + static_cast<uint32_t>(b) * 4096u, &tmC, cbar0 + 8u * b,
+                            col0 + ci * cw, row_base);
+            };
+            const bool job_loads_c = load_c && job.role != JOB_PARTIAL;
+            // The previous job's stores have read their boxes (issued before
+            // this job's accumulator wait, this costs nothing in steady state).
+            if (lane == 0) bulk_wait_group_read<0>();
+            if (job_loads_c && !*abort_flag) {
+                // Prefetch the first C boxes.
+                for (int ci = 0; ci < nchunks && ci < nb; ++ci) {
+                    if (!tma_box(ci)) continue;
+                    if (lane == 0) issue_c(ci);
+                    c_pending |= 1u << (ci % nb);
+                }
+            }
             // One thread waits (for the accumulator and, when finishing a
             // stream-K tile, for the other segments' partials) and tells the
             // other 127 through shared memory: every epilogue thread takes the
@@ -563,29 +562,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!epi_ok[j & 1]) break;
             if (job.role == JOB_FINISH) __threadfence();  // read the partials after the flags
             tc_fence_after();
-            int tm, tn;
-            tile_coords(p, job.tile, tm, tn);
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(acc * p.bn);
-            const int row_base = tm * TILE_M + static_cast<int>(rank) * BM + 32 * q;  // this warp's rows
+            // Partials are kept in the order the threads produce them: float4
+            // i of chunk ci of warp q's lane l at ((q * nchunks + ci) * cw/4 + i) * 32 + l,
+            // so that each warp access is 512 contiguous bytes.
             const size_t my_slot_off = (static_cast<size_t>(unit) * ctas_per_unit + rank) * slot_floats;
-            const int nchunks = p.bn / cw;
-            uint4 c_next[8];
-            if (p.beta != 0.0f && job.role != JOB_PARTIAL)
-                load_c_box(p, row_base, tn * p.bn, lane, c_next);
-            for (int ci = 0; ci < nchunks; ++ci, ++chunk_seq) {
+            for (int ci = 0; ci < nchunks; ++ci) {
                 const int c = ci * cw;
-                const int col_base = tn * p.bn + c;
-                const uint32_t buf = epi_buf0 + static_cast<uint32_t>(q) * 8192u +
-                                     static_cast<uint32_t>(chunk_seq & 1) * 4096u;
-                // The store that last used this buffer has read it.
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                uint4 c_cur[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) c_cur[i] = c_next[i];
-                if (p.beta != 0.0f && job.role != JOB_PARTIAL && ci + 1 < nchunks)
-                    load_c_box(p, row_base, col_base + cw, lane, c_next);  // in flight meanwhile
+                const int col_base = col0 + c;
+                const int b = ci % nb;
+                const uint32_t buf = epi_buf0 + static_cast<uint32_t>(b) * 4096u;
+                const bool via_tma = tma_box(ci);
+                if (!job_loads_c) {
+                    // The store that last used this box has read it.
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
                 float f[64];
                 {
                     uint32_t r[32];
@@ -600,108 +593,128 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int i = 0; i < 32; ++i) f[32 + i] = __uint_as_float(r[i]);
                     }
                 }
+                const size_t part_off = static_cast<size_t>((q * nchunks + ci) * (cw / 4)) * 32 + lane;
                 if (job.role == JOB_PARTIAL) {
                     // Publish this segment's fp32 partial (rows past M too: the
                     // slot is private to this unit).
-                    float4* dst = reinterpret_cast<float4*>(p.ws + my_slot_off +
-                                                            static_cast<size_t>(row_in_cta) * p.bn + c);
+                    float4* dst = reinterpret_cast<float4*>(p.ws + my_slot_off) + part_off;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (i < cw / 4) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                        if (i < cw / 4)
+                            dst[32 * i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
                     continue;
                 }
                 if (job.role == JOB_FINISH) {
                     // acc(k from 0) + partial(unit lo) + ... in unit order.
                     for (int u2 = job.slot_lo; u2 < job.slot_hi; ++u2) {
                         const float4* src = reinterpret_cast<const float4*>(
-                            p.ws + (static_cast<size_t>(u2) * ctas_per_unit + rank) * slot_floats +
-                            static_cast<size_t>(row_in_cta) * p.bn + c);
+                            p.ws + (static_cast<size_t>(u2) * ctas_per_unit + rank) * slot_floats) +
+                                            part_off;
+                        float4 v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (i < cw / 4) v[i] = __ldcg(src + 32 * i);  // written by another SM: read L2
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             if (i < cw / 4) {
-                                const float4 v = __ldcg(src + i);  // written by another SM: read L2
-                                f[4 * i + 0] += v.x;
-                                f[4 * i + 1] += v.y;
-                                f[4 * i + 2] += v.z;
-                                f[4 * i + 3] += v.w;
+                                f[4 * i + 0] += v[i].x;
+                                f[4 * i + 1] += v[i].y;
+                                f[4 * i + 2] += v[i].z;
+                                f[4 * i + 3] += v[i].w;
                             }
                         }
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 64; ++i) f[i] *= p.alpha;
-                if (p.beta != 0.0f) {
-                    // Stage the coalesced C box in the buffer, then read this
-                    // thread's row back: out = alpha*acc + beta*C.
+                if (!via_tma) {
+                    // A box across the N edge (or past M): each thread reads
+                    // and writes the columns of its own row that lie below N.
+                    const int row = row_base + lane;
+                    if (row < p.M && col_base < p.N) {
+                        if (p.out_bf16) {
+                            __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(p.C) +
+                                                static_cast<long long>(row) * p.ldc + col_base;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = 4 * i + (lane >> 3), j = lane & 7;
-                        st_shared_v4(buf + rr * 128 + ((j ^ (rr & 7)) << 4), c_cur[i]);
+                            for (int i = 0; i < 64; ++i) {
+                                if (i < cw && col_base + i < p.N) {
+                                    float o = f[i];
+                                    if (load_c) o = fmaf(p.beta, __bfloat162float(cp[i]), o);
+                                    cp[i] = __float2bfloat16_rn(o);
+                                }
+                            }
+                        } else {
+                            float* cp = static_cast<float*>(p.C) +
+                                        static_cast<long long>(row) * p.ldc + col_base;
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) {
+                                if (i < cw && col_base + i < p.N) {
+                                    float o = f[i];
+                                    if (load_c) o = fmaf(p.beta, cp[i], o);
+                                    cp[i] = o;
+                                }
+                            }
+                        }
                     }
-                    __syncwarp();
+                    continue;
+                }
+                if (load_c) {
+                    // out = alpha*acc + beta*C, C from this thread's row of the box.
+                    bounded_wait<PAIR>(cbar0 + 8u * b, (c_phase >> b) & 1u, abort_flag,
+                                       p.wait_limit_ns, ROLE_EPILOGUE, lt, peer_rank);
+                    c_phase ^= 1u << b;
+                    c_pending &= ~(1u << b);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 u = ld_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4));
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const uint4 u = ld_shared_v4(buf + lane * 128 + ((jj ^ (lane & 7)) << 4));
                         if (cw == 32) {
-                            f[4 * j + 0] = fmaf(p.beta, __uint_as_float(u.x), f[4 * j + 0]);
-                            f[4 * j + 1] = fmaf(p.beta, __uint_as_float(u.y), f[4 * j + 1]);
-                            f[4 * j + 2] = fmaf(p.beta, __uint_as_float(u.z), f[4 * j + 2]);
-                            f[4 * j + 3] = fmaf(p.beta, __uint_as_float(u.w), f[4 * j + 3]);
+                            f[4 * jj + 0] = fmaf(p.beta, __uint_as_float(u.x), f[4 * jj + 0]);
+                            f[4 * jj + 1] = fmaf(p.beta, __uint_as_float(u.y), f[4 * jj + 1]);
+                            f[4 * jj + 2] = fmaf(p.beta, __uint_as_float(u.z), f[4 * jj + 2]);
+                            f[4 * jj + 3] = fmaf(p.beta, __uint_as_float(u.w), f[4 * jj + 3]);
                         } else {
                             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float2 fc = __bfloat1622float2(h[e]);
-                                f[8 * j + 2 * e] = fmaf(p.beta, fc.x, f[8 * j + 2 * e]);
-                                f[8 * j + 2 * e + 1] = fmaf(p.beta, fc.y, f[8 * j + 2 * e + 1]);
+                                f[8 * jj + 2 * e] = fmaf(p.beta, fc.x, f[8 * jj + 2 * e]);
+                                f[8 * jj + 2 * e + 1] = fmaf(p.beta, fc.y, f[8 * jj + 2 * e + 1]);
                             }
                         }
                     }
                 }
-                if (col_base + cw > p.N) {
-                    // A box across the N edge: the tensor store clips columns
-                    // only at 16-byte granularity, so each thread writes its
-                    // row's columns below N itself.
-                    const int row = row_base + lane;
-                    if (row < p.M) {
-                        if (p.out_bf16) {
-                            __nv_bfloat16* cp = static_cast<__nv_bfloat16*>(p.C) +
-                                                static_cast<long long>(row) * p.ldc + col_base;
-#pragma unroll
-                            for (int i = 0; i < 64; ++i)
-                                if (i < cw && col_base + i < p.N) cp[i] = __float2bfloat16_rn(f[i]);
-                        } else {
-                            float* cp = static_cast<float*>(p.C) +
-                                        static_cast<long long>(row) * p.ldc + col_base;
-#pragma unroll
-                            for (int i = 0; i < 64; ++i)
-                                if (i < cw && col_base + i < p.N) cp[i] = f[i];
-                        }
-                    }
-                    continue;
-                }
                 // This thread's row of the box, 128-byte swizzled as the tensor
                 // store expects, then one lane stores the 32-row box.
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int jj = 0; jj < 8; ++jj) {
                     uint4 u;
                     if (cw == 32) {
-                        u = make_uint4(__float_as_uint(f[4 * j]), __float_as_uint(f[4 * j + 1]),
-                                       __float_as_uint(f[4 * j + 2]), __float_as_uint(f[4 * j + 3]));
+                        u = make_uint4(__float_as_uint(f[4 * jj]), __float_as_uint(f[4 * jj + 1]),
+                                       __float_as_uint(f[4 * jj + 2]), __float_as_uint(f[4 * jj + 3]));
                     } else {
                         __nv_bfloat162 h[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            h[e] = __floats2bfloat162_rn(f[8 * j + 2 * e], f[8 * j + 2 * e + 1]);
+                            h[e] = __floats2bfloat162_rn(f[8 * jj + 2 * e], f[8 * jj + 2 * e + 1]);
                         u = *reinterpret_cast<const uint4*>(h);
                     }
-                    st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), u);
+                    st_shared_v4(buf + lane * 128 + ((jj ^ (lane & 7)) << 4), u);
                 }
                 fence_proxy_async_shared();
                 __syncwarp();
-                if (lane == 0 && row_base < p.M && col_base < p.N) {  // boxes past M or N: nothing to store
+                if (lane == 0) {
                     tma_store_2d(&tmC, buf, col_base, row_base);
                     bulk_commit_group();
+                }
+                // Refill the box the previous chunk's store used with C box
+                // ci + nb - 1 once that store has read it.
+                const int nxt = ci + nb - 1;
+                if (job_loads_c && ci >= 1 && nxt < nchunks && tma_box(nxt) && !*abort_flag) {
+                    if (lane == 0) {
+                        bulk_wait_group_read<1>();
+                        issue_c(nxt);
+                    }
+                    c_pending |= 1u << (nxt % nb);
                 }
             }
             tc_fence_before();
@@ -722,6 +735,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else mbar_arrive(tempty_bar(acc));
             }
         }
+        // C copies still in flight after an abort land before the CTA exits.
+        if (lane == 0)
+            for (int b = 0; b < nb; ++b)
+                if ((c_pending >> b) & 1u)
+                    drain_wait(cbar0 + 8u * b, (c_phase >> b) & 1u, p.wait_limit_ns);
     }
 
     if (warp >= 2 && lane == 0) bulk_wait_group_all();  // this warp's C stores are done
@@ -823,10 +841,10 @@ bool smem_attribute(int dev, bool pair) {
     if (!done[dev][pair]) {
         cudaError_t e = pair ? cudaFuncSetAttribute(gemm_tc_kernel<true>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    227 * 1024)
+                                                    kTcMaxSmem)
                              : cudaFuncSetAttribute(gemm_tc_kernel<false>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    227 * 1024);
+                                                    kTcMaxSmem);
         done[dev][pair] = e == cudaSuccess;
     }
     return done[dev][pair];
@@ -954,8 +972,16 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (sms <= 0) return GEMM_ERR_CUDA;
     if (!smem_attribute(dev, pair)) return GEMM_ERR_LAUNCH;
 
-    size_t smem = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) + EPI_BYTES +
-                  sizeof(SharedCtl);
+    // The operand ring, then as many output boxes per epilogue warp (up to
+    // kEpiMaxBufs) as the 227 KB of shared memory leave room for.
+    const size_t base = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) +
+                        sizeof(SharedCtl);
+    const size_t max_smem = kTcMaxSmem;
+    int nb = base < max_smem ? static_cast<int>((max_smem - base) / (4 * EPI_BOX_BYTES)) : 0;
+    if (nb > kEpiMaxBufs) nb = kEpiMaxBufs;
+    if (nb < 2) return GEMM_ERR_UNSUPPORTED;
+    p.epi_bufs = nb;
+    size_t smem = base + static_cast<size_t>(4 * nb) * EPI_BOX_BYTES;
     // One CTA per SM: a 256-wide tile uses all 512 TMEM columns, and a
     // stream-K finisher must never wait on a unit that is itself waiting for
     // TMEM held by another CTA of the same SM.
