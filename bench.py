@@ -95,14 +95,12 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-TILE_NAMES = {128: "128x128x64 (1 SM)", 256: "128x256x64 (1 SM)",
-              512: "256x256x64 (CTA pair, cta_group::2)"}
-TILE_MAX_STAGES = {128: 6, 256: 4, 512: 6}
+TILE_NAMES = {128: "128x128x128 (1 SM)", 256: "128x256x64 (1 SM)",
+              512: "256x256x128 (CTA pair, cta_group::2)"}
+TILE_MAX_STAGES = {128: 3, 256: 4, 512: 3}
 SCHEDULE_NAMES = {0: "automatic", 1: "whole tiles", 2: "stream-K tail"}
-# Default ring depth per tile: the deepest ring that fits, except on the CTA
-# pair, where 5 stages measured fastest in long power-capped runs (4: 1490,
-# 5: 1519, 6: below 5 TFLOP/s).
-TILE_DEFAULT_STAGES = {128: 6, 256: 4, 512: 5}
+# Default ring depth per tile: the deepest ring that fits.
+TILE_DEFAULT_STAGES = {128: 3, 256: 4, 512: 3}
 
 
 def committed_traffic(workload: str, stages: int, tile: int):

@@ -68,7 +68,7 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, c
     if (is_tc(dtype)) {
         r.tile = resolve_tile(M, N, tile);
         if (r.tile == 0) return {GEMM_ERR_ARG, 0};
-        if (stages < 1 || stages > ssp::kTcMaxStages128) return {GEMM_ERR_ARG, 0};
+        if (stages < 1 || stages > ssp::kTcMaxStages) return {GEMM_ERR_ARG, 0};
         if (stages > tile_max_stages(r.tile)) return {GEMM_ERR_UNSUPPORTED, 0};
     } else {
         if (tile != GEMM_SIMT_FRAGMENTS_DOUBLE && tile != GEMM_SIMT_FRAGMENTS_SINGLE)
@@ -269,7 +269,7 @@ int gemm_max_stages(int dtype, int tile) {
                    ? ssp::kSimtMaxStages
                    : GEMM_ERR_ARG;
     if (!is_tc(dtype)) return GEMM_ERR_ARG;
-    if (tile == GEMM_TILE_AUTO) return ssp::kTcMaxStages128;
+    if (tile == GEMM_TILE_AUTO) return ssp::kTcMaxStages;
     const int m = tile_max_stages(tile);
     return m > 0 ? m : GEMM_ERR_ARG;
 }

@@ -27,7 +27,8 @@
 // Ring protocol (slot s = i mod S, n = i div S for the i-th K tile a CTA
 // handles): the producer waits empty[s] for parity (n&1)^1, arms full[s] with
 // the stage's byte count and issues the copies; the MMA thread waits full[s]
-// for parity n&1, issues BK/16 MMAs and commits to empty[s].  With S = 1 the
+// for parity n&1, issues the stage's MMAs (K = 64 * KA per stage, 16 per MMA)
+// and commits to empty[s].  With S = 1 the
 // producer's next copy waits for the MMAs of the same slot: the page's single
 // buffer with a load phase and a compute phase.
 //
@@ -56,11 +57,10 @@ __device__ GemmDeviceStatus g_gemm_status;
 namespace {
 
 constexpr int BM = 128;                 // tile rows = TMEM lanes = UMMA M
-constexpr int BK = 64;                  // 64 x 2 bytes = one 128-byte swizzle row
+constexpr int BK = 64;                  // K of one swizzle atom: 64 x 2 bytes = one 128-byte row
 constexpr int UMMA_K = 16;              // K per tcgen05.mma (kind::f16)
 constexpr int NUM_THREADS = 192;
-constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64 x 64 box, 8 KB
+constexpr int A_ATOM_BYTES = BM * BK * 2;  // 16 KB
 constexpr int EPI_BOX_BYTES = 4096;         // one output box: 32 rows x 128 bytes
 constexpr int kEpiMaxBufs = 4;              // output boxes per epilogue warp, at most
 constexpr int kTcMaxSmem = 227 * 1024;      // dynamic shared memory a CTA may opt in to
@@ -103,7 +103,7 @@ struct Job {
 
 struct SharedCtl {
     // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-    unsigned long long bar[2 * kTcMaxStages128 + 5];
+    unsigned long long bar[2 * kTcMaxStages + 5];
     unsigned long long cbar[4 * kEpiMaxBufs];  // C box copies, per epilogue warp and box
     uint32_t tmem_base;
     int abort;
@@ -259,7 +259,12 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 // both CTAs (multicast), and both epilogues release the accumulator to the
 // leader.  (Relaying the peer's stage through a thread instead costs one
 // remote round trip per stage and capped the pair at ~60 % of the MMA rate.)
-template <bool PAIR>
+//
+// KA = 64-deep K atoms per pipeline stage (K = 64 * KA per stage, 4 * KA MMAs
+// between two ring waits).  Each stage costs the MMA thread one wait and one
+// commit, which on GB300 take about as long as a few MMAs: with 4 MMAs per
+// stage the tensor pipe idled ~15 % of the time, with 8 it stays busy.
+template <bool PAIR, int KA>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -268,9 +273,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
+    constexpr int BKS = KA * BK;                       // K per stage
+    constexpr int A_STAGE_BYTES = KA * A_ATOM_BYTES;
+    constexpr int B_CHUNK_BYTES = 64 * BKS * 2;        // MN-major B: one 64-column chunk of a stage
     const int S = p.stages;
     const int b_cols = PAIR ? p.bn / 2 : p.bn;   // B columns staged by this CTA
-    const int b_stage_bytes = b_cols * BK * 2;
+    const int b_atom_bytes = b_cols * BK * 2;    // K-major B: one 64-deep atom
+    const int b_stage_bytes = KA * b_atom_bytes;
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * A_STAGE_BYTES;
     uint8_t* epi_ring = b_ring + S * b_stage_bytes;  // 4 warps x epi_bufs output boxes
@@ -355,28 +364,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t a_dst = smem_addr(a_ring + s * A_STAGE_BYTES);
                         const uint32_t b_dst = smem_addr(b_ring + s * b_stage_bytes);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), armed_bytes);
+                        // A: KA atoms of 64 K; B: one copy per 64-column chunk
+                        // (MN-major: 128 K rows each) or per 64-deep atom (K-major).
+                        const int k0 = kt * BKS;
                         if (PAIR && !leader) {
                             const uint32_t bar = leader_full0 + 8u * s;
-                            tma_load_2d_pair_hint(a_dst, &tmA, bar, kt * BK, a_row, a_policy);
+#pragma unroll
+                            for (int a = 0; a < KA; ++a)
+                                tma_load_2d_pair_hint(a_dst + a * A_ATOM_BYTES, &tmA, bar, k0 + a * BK,
+                                                      a_row, a_policy);
                             if (p.b_chunked) {
-                                tma_load_3d_pair(b_dst, &tmB, bar, 0, kt * BK, b_col / 64);
+                                tma_load_3d_pair(b_dst, &tmB, bar, 0, k0, b_col / 64);
                             } else if (p.b_mn_major) {
                                 for (int j = 0; j < b_cols / 64; ++j)
-                                    tma_load_2d_pair(b_dst + j * B_BOX_BYTES, &tmB, bar,
-                                                     b_col + 64 * j, kt * BK);
+                                    tma_load_2d_pair(b_dst + j * B_CHUNK_BYTES, &tmB, bar,
+                                                     b_col + 64 * j, k0);
                             } else {
-                                tma_load_2d_pair(b_dst, &tmB, bar, kt * BK, b_col);
+#pragma unroll
+                                for (int a = 0; a < KA; ++a)
+                                    tma_load_2d_pair(b_dst + a * b_atom_bytes, &tmB, bar, k0 + a * BK,
+                                                     b_col);
                             }
                         } else {
-                            tma_load_2d_hint(a_dst, &tmA, full_bar(s), kt * BK, a_row, a_policy);
+#pragma unroll
+                            for (int a = 0; a < KA; ++a)
+                                tma_load_2d_hint(a_dst + a * A_ATOM_BYTES, &tmA, full_bar(s),
+                                                 k0 + a * BK, a_row, a_policy);
                             if (p.b_chunked) {
-                                tma_load_3d(b_dst, &tmB, full_bar(s), 0, kt * BK, b_col / 64);
+                                tma_load_3d(b_dst, &tmB, full_bar(s), 0, k0, b_col / 64);
                             } else if (p.b_mn_major) {
                                 for (int j = 0; j < b_cols / 64; ++j)
-                                    tma_load_2d(b_dst + j * B_BOX_BYTES, &tmB, full_bar(s),
-                                                b_col + 64 * j, kt * BK);
+                                    tma_load_2d(b_dst + j * B_CHUNK_BYTES, &tmB, full_bar(s),
+                                                b_col + 64 * j, k0);
                             } else {
-                                tma_load_2d(b_dst, &tmB, full_bar(s), kt * BK, b_col);
+#pragma unroll
+                                for (int a = 0; a < KA; ++a)
+                                    tma_load_2d(b_dst + a * b_atom_bytes, &tmB, full_bar(s),
+                                                k0 + a * BK, b_col);
                             }
                         }
                     }
@@ -414,14 +438,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // -------------------------------------------------------- MMA issuer
-            const uint32_t a_base = smem_addr(a_ring);
-            const uint32_t b_base = smem_addr(b_ring);
             // K-major operands: 128-byte rows, 8-row groups 1024 bytes apart; one
-            // K=16 step is 32 bytes along the row.  MN-major B: 64-column boxes
-            // 8 KB apart (leading offset), 8-row K groups 1024 bytes apart; one
-            // K=16 step is 16 rows = 2048 bytes.
-            const uint32_t b_lbo = p.b_mn_major ? B_BOX_BYTES : 16u;
-            const uint32_t b_kstep = p.b_mn_major ? 2048u : 32u;
+            // K=16 step is 32 bytes along the row, the next 64-deep atom starts
+            // one atom further on.  MN-major B: 64-column chunks B_CHUNK_BYTES
+            // apart (leading offset), 8-row K groups 1024 bytes apart; one K=16
+            // step is 16 rows = 2048 bytes.
+            // The descriptors of stage 0's first MMA; every other MMA of the
+            // ring only moves the start address (the low 14 bits, in 16-byte
+            // units), which stays below 2^14 for any shared-memory address.
+            const uint64_t a_desc0 = smem_desc(smem_addr(a_ring), 16u, 1024u);
+            const uint64_t b_desc0 =
+                smem_desc(smem_addr(b_ring), p.b_mn_major ? B_CHUNK_BYTES : 16u, 1024u);
+            const uint32_t a_lo = static_cast<uint32_t>(a_desc0);
+            const uint32_t a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+            const uint32_t b_lo = static_cast<uint32_t>(b_desc0);
+            const uint32_t b_hi = static_cast<uint32_t>(b_desc0 >> 32);
+            // B start-address steps (16-byte units) per K=16 and per atom.
+            const uint32_t b_k16 = p.b_mn_major ? 2048u / 16u : 32u / 16u;
+            const uint32_t b_atom16 =
+                p.b_mn_major ? 4u * b_k16 : static_cast<uint32_t>(b_atom_bytes) / 16u;
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -445,12 +480,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_s = a_base + s * A_STAGE_BYTES;
-                    const uint32_t b_s = b_base + s * b_stage_bytes;
+                    const uint32_t a_s = a_lo + static_cast<uint32_t>(s * A_STAGE_BYTES) / 16u;
+                    const uint32_t b_s = b_lo + static_cast<uint32_t>(s * b_stage_bytes) / 16u;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = smem_desc(a_s + kk * 32u, 16u, 1024u);
-                        const uint64_t bd = smem_desc(b_s + kk * b_kstep, b_lbo, 1024u);
+                    for (int kk = 0; kk < BKS / UMMA_K; ++kk) {
+                        const uint32_t ka = static_cast<uint32_t>(kk / 4), k4 = static_cast<uint32_t>(kk % 4);
+                        const uint64_t ad = (static_cast<uint64_t>(a_hi) << 32) |
+                                            (a_s + ka * (A_ATOM_BYTES / 16) + k4 * 2u);
+                        const uint64_t bd = (static_cast<uint64_t>(b_hi) << 32) |
+                                            (b_s + ka * b_atom16 + k4 * b_k16);
                         const uint32_t accum = (kt != job.kb || kk != 0) ? 1u : 0u;
                         if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
                         else umma_f16(d_tmem, ad, bd, p.idesc, accum);
@@ -787,16 +825,17 @@ bool encode_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t rows, uin
 
 // Row-major B (K x N, N a multiple of 64) as a 3-D tensor: 64 columns
 // (contiguous), K rows (stride ld elements), N/64 chunks (stride 64 elements).
-// A box (64, BK, chunks) then lands chunk after chunk, each chunk's BK rows
-// of 128 bytes contiguous and 128-byte swizzled: the MN-major operand layout
-// the MMA reads, filled by one copy instead of one per chunk.
+// A box (64, bks, chunks) then lands chunk after chunk, each chunk's bks rows
+// (the K of one stage) of 128 bytes contiguous and 128-byte swizzled: the
+// MN-major operand layout the MMA reads, filled by one copy instead of one
+// per chunk.
 bool encode_b_chunked(CUtensorMap* map, const void* base, bool bf16, uint64_t K, uint64_t N,
-                      uint64_t ld, uint32_t chunks) {
+                      uint64_t ld, uint32_t chunks, uint32_t bks) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {64, K, N / 64};
     cuuint64_t strides[2] = {ld * 2, 128};
-    cuuint32_t box[3] = {64, BK, chunks};
+    cuuint32_t box[3] = {64, bks, chunks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, const_cast<void*>(base), dims, strides, box, estr,
@@ -832,28 +871,38 @@ int device_sms(int dev) {
     return cache[dev];
 }
 
-// The kernels' dynamic shared-memory limit is a per-device attribute.
-bool smem_attribute(int dev, bool pair) {
-    static std::mutex mu;
-    static bool done[64][2] = {};
-    std::lock_guard<std::mutex> g(mu);
-    if (dev < 0 || dev >= 64) return false;
-    if (!done[dev][pair]) {
-        cudaError_t e = pair ? cudaFuncSetAttribute(gemm_tc_kernel<true>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    kTcMaxSmem)
-                             : cudaFuncSetAttribute(gemm_tc_kernel<false>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    kTcMaxSmem);
-        done[dev][pair] = e == cudaSuccess;
-    }
-    return done[dev][pair];
+// 64-deep K atoms per stage: 2 (K = 128 per stage, 8 MMAs between ring
+// waits) except for the one-CTA 128 x 256 tile, whose 96 KB stages would
+// leave room for only two; it keeps 48 KB stages of K = 64.
+int stage_atoms(bool pair, int bn) { return (!pair && bn == 256) ? 1 : 2; }
+
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
+
+// The kernel instance for a tile and stage depth.
+TcKernel kernel_for(bool pair, int ka) {
+    if (pair) return gemm_tc_kernel<true, 2>;
+    return ka == 1 ? gemm_tc_kernel<false, 1> : gemm_tc_kernel<false, 2>;
 }
 
-void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid,
-                        size_t smem, cudaStream_t stream) {
+// The kernels' dynamic shared-memory limit is a per-device attribute.
+bool smem_attribute(int dev, bool pair, int ka) {
+    static std::mutex mu;
+    static bool done[64][2][2] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64 || ka < 1 || ka > 2) return false;
+    if (!done[dev][pair][ka - 1]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            kernel_for(pair, ka), cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
+        done[dev][pair][ka - 1] = e == cudaSuccess;
+    }
+    return done[dev][pair][ka - 1];
+}
+
+// Launch configuration: clusters of `cluster` CTAs (2 for the pair tile).
+void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int cluster,
+                   size_t smem, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     *cfg = cudaLaunchConfig_t{};
@@ -862,7 +911,7 @@ void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int 
     cfg->dynamicSmemBytes = smem;
     cfg->stream = stream;
     cfg->attrs = attr;
-    cfg->numAttrs = 1;
+    cfg->numAttrs = cluster > 1 ? 1 : 0;
 }
 
 // Number of CTA pairs that can be resident at once for a given shared-memory
@@ -877,9 +926,9 @@ int max_resident_pairs(int dev, size_t smem) {
         if (key_smem[dev][i] == smem && val[dev][i] > 0) return val[dev][i];
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    pair_launch_config(&cfg, attr, 2, smem, nullptr);
+    launch_config(&cfg, attr, 2, 2, smem, nullptr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<true>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, 2), &cfg) != cudaSuccess) n = 0;
     for (int i = 0; i < 8; ++i)
         if (key_smem[dev][i] == 0 || i == 7) {
             key_smem[dev][i] = smem;
@@ -894,6 +943,7 @@ struct Geometry {
     int cluster = 1;   // CTAs per cluster
     size_t smem = 0;   // dynamic shared memory per CTA
     int units = 0;     // persistent workers (CTAs, or CTA pairs)
+    int ka = 2;        // 64-deep K atoms per stage
     size_t ws_bytes = 0;  // stream-K workspace (partials + flags), 0 if unused
 };
 
@@ -940,7 +990,10 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.tiles_m = static_cast<int>((L.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<int>((L.N + bn - 1) / bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.k_tiles = static_cast<int>((L.K + BK - 1) / BK);
+    const int ka = stage_atoms(pair, bn);
+    const int bks = ka * BK;
+    geo.ka = ka;
+    p.k_tiles = static_cast<int>((L.K + bks - 1) / bks);
     p.group_m = pair ? 8 : 16;
     p.stages = S;
     p.bn = bn;
@@ -970,11 +1023,11 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
     const int sms = device_sms(dev);
     if (sms <= 0) return GEMM_ERR_CUDA;
-    if (!smem_attribute(dev, pair)) return GEMM_ERR_LAUNCH;
+    if (!smem_attribute(dev, pair, ka)) return GEMM_ERR_LAUNCH;
 
     // The operand ring, then as many output boxes per epilogue warp (up to
     // kEpiMaxBufs) as the 227 KB of shared memory leave room for.
-    const size_t base = 1024 + static_cast<size_t>(S) * (A_STAGE_BYTES + b_cols * BK * 2) +
+    const size_t base = 1024 + static_cast<size_t>(S) * (ka * A_ATOM_BYTES + b_cols * bks * 2) +
                         sizeof(SharedCtl);
     const size_t max_smem = kTcMaxSmem;
     int nb = base < max_smem ? static_cast<int>((max_smem - base) / (4 * EPI_BOX_BYTES)) : 0;
@@ -1017,33 +1070,43 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     return GEMM_OK;
 }
 
+// Tensor maps of one call.  A: M x K row-major, boxes of 64 (K) x 128 (M).
+// B column-major (N x K row-major): boxes of 64 (K) x b_cols (N).  B
+// row-major: one 3-D box of b_cols/64 chunks per stage when N is a multiple
+// of 64 and `chunked` is allowed, else boxes of 64 (N) x bks (K), b_cols/64
+// of them per stage.
+bool encode_maps(const TcLaunch& L, int bks, bool chunked, CUtensorMap* tmA, CUtensorMap* tmB,
+                 CUtensorMap* tmC, int* b_chunked) {
+    const int b_cols = L.pair ? L.tile_n / 2 : L.tile_n;
+    if (!encode_c(tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return false;
+    if (!encode_2d(tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return false;
+    *b_chunked = (chunked && !L.b_col_major && L.N % 64 == 0) ? 1 : 0;
+    if (L.b_col_major) return encode_2d(tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols);
+    if (*b_chunked) return encode_b_chunked(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, b_cols / 64, bks);
+    return encode_2d(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, bks);
+}
+
+int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                  const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    launch_config(&cfg, attr, geo.grid, geo.cluster, geo.smem, stream);
+    if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.ka), tmA, tmB, tmC, p) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
 }  // namespace
 
 int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
     const int bn = L.tile_n;
-    const int b_cols = pair ? bn / 2 : bn;
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_c(&tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return GEMM_ERR_LAUNCH;
-    // A: M x K row-major, boxes of 64 (K) x 128 (M).
-    if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
-    const bool b_chunked = !L.b_col_major && L.N % 64 == 0;
-    if (L.b_col_major) {
-        // B column-major = N x K row-major: boxes of 64 (K) x b_cols (N).
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
-    } else if (b_chunked) {
-        // B row-major, N a multiple of 64: one 3-D box of b_cols/64 chunks per stage.
-        if (!encode_b_chunked(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, b_cols / 64))
-            return GEMM_ERR_LAUNCH;
-    } else {
-        // B row-major K x N: boxes of 64 (N) x 64 (K); b_cols/64 boxes per stage.
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
-    }
     TcParams p;
     Geometry geo;
     int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
-    p.b_chunked = b_chunked ? 1 : 0;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_maps(L, geo.ka * BK, true, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
     if (geo.ws_bytes) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -1054,16 +1117,7 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
         p.ws = static_cast<float*>(ws);
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
     }
-    if (!pair) {
-        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, tmC, p);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-    }
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, tmC, p) != cudaSuccess)
-        return GEMM_ERR_LAUNCH;
-    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    return launch_kernel(geo, pair, tmA, tmB, tmC, p, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -1096,19 +1150,12 @@ int noalloc_scratch_address(int dev, void** out) {
 int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
     const int bn = L.tile_n;
-    const int b_cols = pair ? bn / 2 : bn;
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_c(&tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return GEMM_ERR_LAUNCH;
-    if (!encode_2d(&tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return GEMM_ERR_LAUNCH;
-    if (L.b_col_major) {
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols)) return GEMM_ERR_LAUNCH;
-    } else {
-        if (!encode_2d(&tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK)) return GEMM_ERR_LAUNCH;
-    }
     TcParams p;
     Geometry geo;
     int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_maps(L, geo.ka * BK, false, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
     if (geo.ws_bytes) {
         if (geo.ws_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH;
         int dev = 0;
@@ -1124,16 +1171,7 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
         p.ws = static_cast<float*>(ws);
         p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
     }
-    if (!pair) {
-        gemm_tc_kernel<false><<<geo.grid, NUM_THREADS, geo.smem, stream>>>(tmA, tmB, tmC, p);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
-    }
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    pair_launch_config(&cfg, attr, geo.grid, geo.smem, stream);
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, tmA, tmB, tmC, p) != cudaSuccess)
-        return GEMM_ERR_LAUNCH;
-    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    return launch_kernel(geo, pair, tmA, tmB, tmC, p, stream);
 }
 
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {

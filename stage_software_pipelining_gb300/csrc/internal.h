@@ -81,9 +81,12 @@ int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float
 int copy_launch(void* dst, const void* src, int64_t n_bytes, int stages, cudaStream_t stream);
 constexpr int kCopyMaxStages = 8;
 
-constexpr int kTcMaxStages128 = 6;   // 128 x 128 tile: 32 KB per stage
-constexpr int kTcMaxStages256 = 4;   // 128 x 256 tile: 48 KB per stage
-constexpr int kTcMaxStagesPair = 6;  // 256 x 256 tile on a CTA pair: 32 KB per stage per CTA
+// Tensor-core ring depth limits.  A stage holds K = 128 of both operands
+// (K = 64 for the 128 x 256 tile).
+constexpr int kTcMaxStages128 = 3;   // 128 x 128 x 128 tile: 64 KB per stage
+constexpr int kTcMaxStages256 = 4;   // 128 x 256 x 64 tile: 48 KB per stage
+constexpr int kTcMaxStagesPair = 3;  // 256 x 256 x 128 tile on a CTA pair: 64 KB per stage per CTA
+constexpr int kTcMaxStages = 4;      // the largest of the three
 constexpr int kSimtMaxStages = 4;
 
 }  // namespace ssp

@@ -49,7 +49,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def gemm_ex(lib, M, N, K, A=P, lda=None, B=P, ldb=None, C=P, ldc=None, alpha=1.0, beta=0.0,
-            dtype=GEMM_BF16_F32, stages=4, bcm=0, tile=0):
+            dtype=GEMM_BF16_F32, stages=3, bcm=0, tile=0):
     lda = K if lda is None else lda
     ldb = (K if bcm else N) if ldb is None else ldb
     ldc = N if ldc is None else ldc
@@ -69,8 +69,11 @@ def test_bad_dtype_and_stages(lib):
     assert gemm_ex(lib, 8, 8, 8, stages=0) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, stages=7) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=5) == G.GEMM_ERR_ARG
-    # 128 x 256 tiles hold at most 4 stages in shared memory
-    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_128x256) == G.GEMM_ERR_UNSUPPORTED
+    # shared memory holds at most 3 stages of K = 128 for the 128 x 128 and
+    # pair tiles and 4 of K = 64 for the 128 x 256 tile; no tile takes 5
+    assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_256x256_2SM) == G.GEMM_ERR_UNSUPPORTED
+    assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_128x128) == G.GEMM_ERR_UNSUPPORTED
+    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_128x256) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, tile=192) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, tile=1024) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=128) == G.GEMM_ERR_ARG
@@ -133,17 +136,17 @@ def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_F32, 0) == 4
     assert lib.gemm_max_stages(GEMM_F32, 1) == 4      # single register fragment set
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
-    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 6
-    assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 6
-    assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 6
+    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 3
+    assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 3
+    assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 4
     assert lib.gemm_max_stages(GEMM_F32, 128) == G.GEMM_ERR_ARG
     assert lib.gemm_max_stages(9, 0) == G.GEMM_ERR_ARG
 
 
 def test_host_entry_validates_first(lib):
-    assert lib.gemm_host(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+    assert lib.gemm_host(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0,
                          None) == G.GEMM_ERR_ARG
-    assert lib.gemm_host(0, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+    assert lib.gemm_host(0, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0,
                          None) == G.GEMM_OK
 
 
@@ -197,11 +200,11 @@ def test_schedule_hook(lib):
 def test_noalloc_entry_validates_on_the_host(lib):
     na = lib.gemm_noalloc
     # the same argument checks as gemm_ex, answered before any CUDA call
-    assert na(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0, None) == G.GEMM_ERR_ARG
-    assert na(8, 16, 24, P + 2, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0,
+    assert na(-1, 8, 8, P, 8, P, 8, P, 8, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0, None) == G.GEMM_ERR_ARG
+    assert na(8, 16, 24, P + 2, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0,
               None) == G.GEMM_ERR_ALIGN
     # the SIMT path has no scratch, so no allocation-free variant
     assert na(8, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_F32, 2, 0, 0,
               None) == G.GEMM_ERR_UNSUPPORTED
-    assert na(0, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 4, 0, 0, None) == G.GEMM_OK
+    assert na(0, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0, None) == G.GEMM_OK
     assert "fixed array" in lib.gemm_status_string(G.GEMM_ERR_SCRATCH).decode()

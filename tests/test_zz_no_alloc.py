@@ -48,9 +48,9 @@ def call(fn, A, B, C, alpha, beta, dtype, stages, tile):
 CASES = [
     # (base workload, M, N, K, tile, stages): fewer or ragged tiles than units,
     # so the stream-K tail runs and uses the fixed array
-    ("bf16_8192_beta1", 1100, 904, 4096, G.TILE_256x256_2SM, 4),
+    ("bf16_8192_beta1", 1100, 904, 4096, G.TILE_256x256_2SM, 3),
     ("bf16_8192_beta1", 700, 1000, 1504, G.TILE_128x256, 3),
-    ("bf16_ragged_colB", 1000, 1200, 2048, G.TILE_256x256_2SM, 6),
+    ("bf16_ragged_colB", 1000, 1200, 2048, G.TILE_256x256_2SM, 2),
 ]
 
 
@@ -94,7 +94,7 @@ def test_noalloc_matches_oracle_at_the_headline_shape(lib):
     inp = make_inputs(w)
     A, B = inp.A.cuda(), inp.B.cuda()
     C = inp.C0.cuda()
-    st = call(lib.gemm_noalloc, A, B, C, w.alpha, w.beta, w.dtype, 4, G.TILE_256x256_2SM)
+    st = call(lib.gemm_noalloc, A, B, C, w.alpha, w.beta, w.dtype, 3, G.TILE_256x256_2SM)
     assert st == G.GEMM_OK, G.status_string(st)
     torch.cuda.synchronize()
     rng = np.random.default_rng(3)
