@@ -18,6 +18,8 @@
  * a load phase and a compute phase per K tile, stages = 2 is double
  * buffering, stages >= 3 is a multi-stage ring.  The stage count changes
  * timing only: for one dtype and tile, every stage count gives bit-identical C.
+ * A tensor-core stage holds a K slice of 128 (of 64 for the 128 x 256 tile)
+ * of both operands: 8 (4) tcgen05.mma instructions per ring wait.
  *
  * Layout (all row-major, leading dimensions in elements):
  *   A  M x K, element (i,k) at A[i*lda + k], lda >= K
@@ -27,9 +29,10 @@
  *
  * Types (`dtype`, input -> output; accumulation is always fp32):
  *   GEMM_F32        fp32 A, B, C      CUDA-core SIMT sgemm, stages 1..4
- *   GEMM_F16_F32    fp16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
- *   GEMM_BF16_F32   bf16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
- *   GEMM_BF16_BF16  bf16 A, B, C      tcgen05 tensor cores, stages 1..6;
+ *   GEMM_F16_F32    fp16 A, B; fp32 C tcgen05 tensor cores, stages 1..3 or 1..4
+ *   GEMM_BF16_F32   bf16 A, B; fp32 C tcgen05 tensor cores, stages 1..3 or 1..4
+ *   GEMM_BF16_BF16  bf16 A, B, C      tcgen05 tensor cores, stages 1..3 or 1..4
+ *                                     (by tile, see gemm_tile_t);
  *                                     fp32 result rounded to nearest even
  *   alpha and beta are fp32.  alpha is applied to the fp32 sum, then beta*C
  *   is added (one fp32 multiply-add per element).
@@ -75,13 +78,15 @@ typedef enum {
 
 /* Tensor-core tile (gemm_ex's `tile`).  The 2-SM tile runs on a cluster of
  * two CTAs with tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and
- * 128 columns of B per K step and holds 128 rows of the 256 x 256 result. */
+ * 128 columns of B per K step and holds 128 rows of the 256 x 256 result.
+ * The stage limits are what fits in 227 KB of shared memory per CTA. */
 typedef enum {
     GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128,
                                     else 128x128 (N <= 128) or 128x256 */
-    GEMM_TILE_128x128 = 128,     /* one CTA, stages 1..6 (32 KB per stage) */
-    GEMM_TILE_128x256 = 256,     /* one CTA, stages 1..4 (48 KB per stage) */
-    GEMM_TILE_256x256_2SM = 512  /* a CTA pair, stages 1..6 (32 KB per stage per CTA) */
+    GEMM_TILE_128x128 = 128,     /* one CTA, K = 128 per stage, stages 1..3 (64 KB each) */
+    GEMM_TILE_128x256 = 256,     /* one CTA, K = 64 per stage, stages 1..4 (48 KB each) */
+    GEMM_TILE_256x256_2SM = 512  /* a CTA pair, K = 128 per stage, stages 1..3
+                                    (64 KB each per CTA) */
 } gemm_tile_t;
 
 /* Register-fragment scheme of the SIMT sgemm (gemm_ex's `tile` when dtype
@@ -111,8 +116,8 @@ typedef enum {
  *   C, ldc     device pointer and leading dimension of C (M x N), read when
  *              beta != 0 and written
  *   dtype      a gemm_dtype_t
- *   stages     depth of the shared-memory ring: 1..6 on the tensor-core path,
- *              1..4 on the SIMT path
+ *   stages     depth of the shared-memory ring: 1..3 on the tensor-core path
+ *              (1..4 for the 128 x 256 tile), 1..4 on the SIMT path
  *   stream     cudaStream_t
  * The tensor-core tile is GEMM_TILE_AUTO's choice.
  */
