@@ -95,13 +95,15 @@ def status_string(status: int) -> str:
         return f"status {status}"
 
 
+_DTYPE_CODES = {(torch.float32, torch.float32): GEMM_F32,
+                (torch.float16, torch.float32): GEMM_F16_F32,
+                (torch.bfloat16, torch.float32): GEMM_BF16_F32,
+                (torch.bfloat16, torch.bfloat16): GEMM_BF16_BF16}
+
+
 def dtype_code(a_dtype: torch.dtype, c_dtype: torch.dtype) -> int:
-    table = {(torch.float32, torch.float32): GEMM_F32,
-             (torch.float16, torch.float32): GEMM_F16_F32,
-             (torch.bfloat16, torch.float32): GEMM_BF16_F32,
-             (torch.bfloat16, torch.bfloat16): GEMM_BF16_BF16}
     try:
-        return table[(a_dtype, c_dtype)]
+        return _DTYPE_CODES[(a_dtype, c_dtype)]
     except KeyError:
         raise ValueError(f"unsupported type pair {a_dtype} -> {c_dtype}") from None
 
@@ -161,17 +163,21 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
     fp32 SIMT path.
     Raises GemmError on a non-OK status.  Returns C.
     """
-    for t, n in ((A, "A"), (B, "B"), (C, "C")):
-        if t.device.type != "cuda":
-            raise ValueError(f"{n} must be a CUDA tensor (use gemm_host for host buffers)")
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("A, B and C must be CUDA tensors (use gemm_host for host buffers)")
     M, N, K, lda, ldb, bcm, ldc, code = _args(A, B, C)
     st = default_stages(code) if stages is None else int(stages)
-    s = (stream or torch.cuda.current_stream(C.device)).cuda_stream
-    lib = load_library()
+    dev = C.device.index
+    s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+    lib = _lib or load_library()
     fn = lib.gemm_checked if checked else lib.gemm_ex
-    with torch.cuda.device(C.device):
-        status = fn(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
-                    float(alpha), float(beta), code, st, bcm, int(tile), s)
+    args = (M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+            float(alpha), float(beta), code, st, bcm, int(tile), s)
+    if dev == torch.cuda.current_device():
+        status = fn(*args)
+    else:
+        with torch.cuda.device(dev):
+            status = fn(*args)
     if status != GEMM_OK:
         raise GemmError(status, "gemm_checked" if checked else "gemm_ex")
     return C

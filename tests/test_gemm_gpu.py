@@ -149,6 +149,21 @@ def test_tc_shape_fuzz(shape, b_col_major):
 
 
 @pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("b_col_major", [False, True])
+def test_tc_k_tails_across_the_atoms_of_a_stage(tile, b_col_major):
+    """A stage holds K = 128 as two 64-deep atoms (K = 64 on the 128 x 256
+    tile): K ends inside the first atom, exactly at an atom or stage edge,
+    and inside the second atom, so that one copy of a stage is partly or
+    wholly past K (zero fill).  beta = 1 exercises the C box copies too."""
+    for K in (8, 56, 64, 72, 120, 128, 136, 192, 200, 248, 256, 264):
+        inp = make_inputs(workload(GEMM_BF16_F32, 200, 300, K, b_col_major=b_col_major, beta=1.0))
+        out, _ = run_gpu(inp, 2, tile=tile)
+        ref, absb = oracle_full(inp)
+        check_against_oracle(out, ref, absb, GEMM_BF16_F32, beta=1.0, C0=inp.C0,
+                             what=f"K tail K={K} tile={tile} colB={b_col_major}")
+
+
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("dtype", TC_DTYPES)
 def test_tc_stage_invariance_bitwise(tile, dtype):
     """The ring depth changes timing only: every stage count gives the same bits."""
