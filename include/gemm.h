@@ -149,19 +149,26 @@ int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 
 /*
  * gemm_host -- the same operation on HOST buffers: copies A, B (and C when
- * beta != 0) to the device, runs gemm_ex on `stream`, copies C back and
- * synchronises.  Device staging buffers are allocated on first use and
- * cached per device (grown when a larger problem arrives); pinned host memory
- * makes the copies asynchronous DMA.  Leading dimensions are kept as given.
+ * beta != 0) to the device, runs gemm_ex, copies C back and synchronises.
+ * The copies are pipelined with the computation: B goes first, then M is cut
+ * into up to 8 row panels (whole 256-row tiles); panel p's rows of A and C
+ * are copied in on an internal stream while panel p-1 is computed on
+ * `stream` and earlier panels' C rows are copied back on a second internal
+ * stream.  Every panel gives the same bits as one gemm_ex over all of M.
+ * Work queued on `stream` before the call runs first.  Device staging
+ * buffers, the two streams and their events are created on first use and
+ * cached per device (buffers grow when a larger problem arrives); pinned
+ * host memory makes the copies asynchronous DMA.  Leading dimensions are kept
+ * as given.  Calls from several threads run one at a time.
  */
 int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
               int b_col_major, int tile, void* stream);
 
-/* Frees the device buffers the library caches on the current device:
- * gemm_host's staging buffers and the stream-K workspaces (gemm_schedule_set
- * mode 2).  Call it when no GEMM of this library is running on the device;
- * later calls allocate again as needed. */
+/* Frees what the library caches on the current device: gemm_host's staging
+ * buffers, copy streams and events, and the stream-K workspaces
+ * (gemm_schedule_set mode 2).  Call it when no GEMM of this library is
+ * running on the device; later calls create them again as needed. */
 int gemm_host_release(void);
 
 /* Human-readable name of a gemm_status_t (static storage). */

@@ -5,6 +5,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/gemm.h"
@@ -147,6 +148,51 @@ struct Staging {
 std::mutex g_staging_mu;
 Staging g_staging[64];
 
+// gemm_host's copy streams and events, created on first use per device.
+constexpr int kHostPanels = 8;  // row panels a large gemm_host call is cut into
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;  // host->device and device->host copies
+    cudaEvent_t start = nullptr, b_done = nullptr, done = nullptr;
+    cudaEvent_t in_done[kHostPanels] = {}, gemm_done[kHostPanels] = {};
+};
+HostPipe g_pipe[64];
+
+int host_pipe(int dev, HostPipe** out) {
+    HostPipe& p = g_pipe[dev];
+    if (!p.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.start, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.b_done, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p.done, ef) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        for (int i = 0; i < kHostPanels; ++i)
+            if (cudaEventCreateWithFlags(&p.in_done[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&p.gemm_done[i], ef) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        p.ready = true;
+    }
+    *out = &p;
+    return GEMM_OK;
+}
+
+void host_pipe_release(int dev) {
+    HostPipe& p = g_pipe[dev];
+    if (!p.ready) return;
+    cudaStreamSynchronize(p.in);
+    cudaStreamSynchronize(p.out);
+    cudaStreamDestroy(p.in);
+    cudaStreamDestroy(p.out);
+    for (cudaEvent_t e : {p.start, p.b_done, p.done}) cudaEventDestroy(e);
+    for (int i = 0; i < kHostPanels; ++i) {
+        cudaEventDestroy(p.in_done[i]);
+        cudaEventDestroy(p.gemm_done[i]);
+    }
+    p = HostPipe{};
+}
+
 int staging_get(int dev, int which, size_t bytes, void** out) {
     Staging& s = g_staging[dev];
     if (s.cap[which] < bytes) {
@@ -206,30 +252,78 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GEMM_ERR_CUDA;
     const size_t si = in_size(dtype), so = out_size(dtype);
     const bool need_ab = K > 0 && alpha != 0.0f;
-    const size_t a_bytes = need_ab ? (static_cast<size_t>(M - 1) * lda + K) * si : 0;
     const size_t b_bytes =
         need_ab ? (b_col_major ? static_cast<size_t>(N - 1) * ldb + K
                                : static_cast<size_t>(K - 1) * ldb + N) * si
                 : 0;
-    const size_t c_bytes = (static_cast<size_t>(M - 1) * ldc + N) * so;
+    // Bytes of rows [r0, r1) of a row-major operand with leading dimension ld.
+    auto rows_bytes = [](int64_t r0, int64_t r1, int64_t ld, int64_t cols, size_t size) {
+        return (static_cast<size_t>(r1 - r0 - 1) * ld + cols) * size;
+    };
+    const size_t a_bytes = need_ab ? rows_bytes(0, M, lda, K, si) : 0;
+    const size_t c_bytes = rows_bytes(0, M, ldc, N, so);
     std::lock_guard<std::mutex> g(g_staging_mu);
     void *dA = nullptr, *dB = nullptr, *dC = nullptr;
     int st;
     if (a_bytes && (st = staging_get(dev, 0, a_bytes, &dA)) != GEMM_OK) return st;
     if (b_bytes && (st = staging_get(dev, 1, b_bytes, &dB)) != GEMM_OK) return st;
     if ((st = staging_get(dev, 2, c_bytes, &dC)) != GEMM_OK) return st;
-    if (a_bytes && cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(dev, &hp)) != GEMM_OK) return st;
+
+    // The copies themselves are pipelined with the GEMM: B goes over first,
+    // then M is cut into row panels; panel p's A and C rows are copied in on
+    // one stream while panel p-1 is computed on the caller's stream and the
+    // C rows of earlier panels are copied back on a third.  Host->device and
+    // device->host copies use the link in both directions at once.  Each
+    // panel is a whole number of 256-row tiles.
+    const int64_t panel_rows = std::max<int64_t>(256, (M + kHostPanels - 1) / kHostPanels + 255) / 256 * 256;
+    const int panels = static_cast<int>((M + panel_rows - 1) / panel_rows);
+    auto fail = [&]() {
+        cudaStreamSynchronize(hp->in);
+        cudaStreamSynchronize(s);
+        cudaStreamSynchronize(hp->out);
         return GEMM_ERR_CUDA;
-    if (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    if (beta != 0.0f && cudaMemcpyAsync(dC, C, c_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    st = run(M, N, K, need_ab ? dA : A, lda, need_ab ? dB : B, ldb, dC, ldc, alpha, beta, dtype,
-             stages, b_col_major, tile, s);
-    if (st != GEMM_OK) return st;
-    if (cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
+    };
+    // Work already queued on the caller's stream comes first.
+    if (cudaEventRecord(hp->start, s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+        return fail();
+    if (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+        return fail();
+    for (int pi = 0; pi < panels; ++pi) {
+        const int64_t r0 = pi * panel_rows, r1 = std::min<int64_t>(M, r0 + panel_rows);
+        char* pA = static_cast<char*>(dA) + static_cast<size_t>(r0) * lda * si;
+        char* pC = static_cast<char*>(dC) + static_cast<size_t>(r0) * ldc * so;
+        const char* hA = static_cast<const char*>(A) + static_cast<size_t>(r0) * lda * si;
+        char* hC = static_cast<char*>(C) + static_cast<size_t>(r0) * ldc * so;
+        const size_t pc_bytes = rows_bytes(r0, r1, ldc, N, so);
+        if (need_ab && cudaMemcpyAsync(pA, hA, rows_bytes(r0, r1, lda, K, si),
+                                       cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+            return fail();
+        if (beta != 0.0f &&
+            cudaMemcpyAsync(pC, hC, pc_bytes, cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+            return fail();
+        if (cudaEventRecord(hp->in_done[pi], hp->in) != cudaSuccess ||
+            cudaStreamWaitEvent(s, hp->in_done[pi], 0) != cudaSuccess)
+            return fail();
+        st = run(r1 - r0, N, K, need_ab ? pA : hA, lda, need_ab ? dB : B, ldb, pC, ldc, alpha,
+                 beta, dtype, stages, b_col_major, tile, s);
+        if (st != GEMM_OK) {
+            fail();
+            return st;
+        }
+        if (cudaEventRecord(hp->gemm_done[pi], s) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->out, hp->gemm_done[pi], 0) != cudaSuccess ||
+            cudaMemcpyAsync(hC, pC, pc_bytes, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+            return fail();
+    }
+    // The caller's stream ends after the last copy back.
+    if (cudaEventRecord(hp->done, hp->out) != cudaSuccess ||
+        cudaStreamWaitEvent(s, hp->done, 0) != cudaSuccess)
+        return fail();
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail();
     return GEMM_OK;
 }
 
@@ -244,6 +338,7 @@ int gemm_host_release(void) {
             s.ptr[i] = nullptr;
             s.cap[i] = 0;
         }
+        host_pipe_release(dev);
     }
     return ssp::tc_release_workspaces();
 }
