@@ -532,6 +532,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t epi_buf0 = smem_addr(epi_ring) + static_cast<uint32_t>(q * nb) * 4096u;
         const uint32_t cbar0 = smem_addr(&ctl->cbar[q * kEpiMaxBufs]);
         const bool load_c = p.beta != 0.0f;
+        // beta = 1 with fp32 C: the box of alpha*acc is added into C at L2 by
+        // a tensor reduce instead of C being read in (one fp32 add per
+        // element, the same value as fmaf(1, C, alpha*acc)).
+        const bool reduce_c = p.beta == 1.0f && !p.out_bf16;
         uint32_t c_phase = 0;    // bit b: parity of the next C copy into box b
         uint32_t c_pending = 0;  // bit b: a C copy into box b is issued and not yet consumed
         int lt = 0;
@@ -556,7 +560,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_load_2d(epi_buf0 + static_cast<uint32_t>(b) * 4096u, &tmC, cbar0 + 8u * b,
                             col0 + ci * cw, row_base);
             };
-            const bool job_loads_c = load_c && job.role != JOB_PARTIAL;
+            const bool job_loads_c = load_c && !reduce_c && job.role != JOB_PARTIAL;
             // The previous job's stores have read their boxes (issued before
             // this job's accumulator wait, this costs nothing in steady state).
             if (lane == 0) bulk_wait_group_read<0>();
@@ -696,7 +700,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     continue;
                 }
-                if (load_c) {
+                if (job_loads_c) {
                     // out = alpha*acc + beta*C, C from this thread's row of the box.
                     bounded_wait<PAIR>(cbar0 + 8u * b, (c_phase >> b) & 1u, abort_flag,
                                        p.wait_limit_ns, ROLE_EPILOGUE, lt, peer_rank);
@@ -741,7 +745,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmC, buf, col_base, row_base);
+                    if (reduce_c) tma_reduce_add_2d(&tmC, buf, col_base, row_base);
+                    else tma_store_2d(&tmC, buf, col_base, row_base);
                     bulk_commit_group();
                 }
                 // Refill the box the previous chunk's store used with C box

@@ -100,6 +100,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
 // 2-D tiled bulk tensor copy shared -> global (completion through the bulk
 // async-group of the issuing thread).  Parts of the box outside the tensor
 // are not written.
+// Add a shared-memory box into global memory element by element
+// (cp.reduce.async.bulk.tensor .add): the add happens at L2, so C is never
+// read into the SM.  For f32 it rounds to nearest once and keeps subnormals
+// (checked on GB300 against fmaf(1, C, x)), i.e. C + x as one fp32 add.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int32_t c0,
+                                                  int32_t c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t c0, int32_t c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(

@@ -193,6 +193,28 @@ def test_tc_alpha_beta(alpha, beta, dtype, tile):
                          what=f"alpha={alpha} beta={beta}")
 
 
+@pytest.mark.parametrize("tile", TILES)
+def test_beta_one_adds_c_with_one_fp32_rounding(tile):
+    """With beta = 1 and fp32 C the epilogue adds alpha*acc into C at L2
+    (tensor reduce): the result must be C0 + (the beta = 0 result) with one
+    fp32 rounding, bit for bit, also for subnormal C0 and a ragged N edge."""
+    M, N, K = 300, 1000, 264
+    inp = make_inputs(workload(GEMM_BF16_F32, M, N, K, beta=1.0))
+    A = to_device_padded(inp.A)
+    B = to_device_padded(inp.B)
+    C0 = inp.C0.cuda()
+    C0[:7] *= 1e-39                                   # subnormal rows
+    prod = torch.zeros(M, N, device="cuda")
+    G.gemm(A, B, prod, 1.5, 0.0, stages=2, tile=tile, checked=True)
+    C = C0.clone()
+    G.gemm(A, B, C, 1.5, 1.0, stages=2, tile=tile, checked=True)
+    assert torch.equal(C, C0 + prod)
+    # A = 0: C0, subnormals included, comes back unchanged
+    Cz = C0.clone()
+    G.gemm(torch.zeros_like(A), B, Cz, 1.0, 1.0, stages=2, tile=tile, checked=True)
+    assert torch.equal(Cz, C0)
+
+
 @pytest.mark.parametrize("dtype", [GEMM_F32] + TC_DTYPES)
 def test_beta_zero_does_not_read_c(dtype):
     inp = make_inputs(workload(dtype, 140, 136, 40, beta=0.0))
