@@ -1058,8 +1058,9 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     const int sk_tiles = T < U ? T : rem;
     // Automatic scheduling uses whole tiles: measured on GB300 the stream-K
     // fix-up (a second epilogue per unit that publishes, then reduces its
-    // partial through the workspace) costs more than the idle tail it removes
-    // (8192^3: 1496 vs 1528 TFLOP/s; 2048^3: 340 vs 695).
+    // partial through the workspace) gains nothing over the idle tail it
+    // removes under the power cap (8192^3: 1622-1624 vs 1628-1629 TFLOP/s in
+    // 2000-step runs) and loses where every tile is split (2048^3).
     const bool use_sk = L.schedule == 2 && rem != 0 && static_cast<long long>(sk_tiles) * KT >= U;
     if (use_sk) {
         p.dp_tiles = T - sk_tiles;

@@ -27,7 +27,7 @@ struct TcLaunch {
     int in_bf16;      // 0 fp16 inputs, 1 bf16 inputs
     int out_bf16;     // 0 fp32 output, 1 bf16 output
     int b_col_major;  // 0 B row-major (N contiguous), 1 B column-major (K contiguous)
-    int stages;       // 1..6
+    int stages;       // ring depth (1..3, or 1..4 for the 128 x 256 tile)
     int tile_n;       // tile width: 128 or 256
     int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256
     int schedule;     // 0 auto, 1 full tiles only, 2 stream-K tail whenever a round is partial
