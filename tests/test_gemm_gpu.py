@@ -310,8 +310,8 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
 # --------------------------------------------------------------------------- full-size workloads
 def sample_indices(M, N, count, seed):
     rng = np.random.default_rng(seed)
-    edge_r = [0, 1, 127, 128, M // 2, M - 2, M - 1]
-    edge_c = [0, 1, 15, 16, 255, 256, N // 2, N - 2, N - 1]
+    edge_r = [r for r in (0, 1, 127, 128, M // 2, M - 2, M - 1) if 0 <= r < M]
+    edge_c = [c for c in (0, 1, 15, 16, 255, 256, N // 2, N - 2, N - 1) if 0 <= c < N]
     rows = [r for r in edge_r for _ in edge_c]
     cols = [c for _ in edge_r for c in edge_c]
     rows += list(rng.integers(0, M, count))
@@ -368,6 +368,53 @@ def test_full_size_stage_sweep_is_bitwise_invariant():
                 base = C
             else:
                 assert torch.equal(C, base), f"tile={tile} stages={s}"
+
+
+@pytest.mark.parametrize("M,N,K", [(1_048_581, 136, 40),    # 4097 pair-tile rows, ragged
+                                   (130, 200, 131_080)])    # 1025 stages of K = 128
+def test_extreme_dimensions_sampled(M, N, K):
+    """Very tall and very deep problems: tile indices, TMA row coordinates,
+    64-bit C offsets and long accumulation chains, checked on sampled
+    entries (the oracle computes each one as a K-term dot product)."""
+    w = workload(GEMM_BF16_F32, M, N, K, beta=1.0)
+    inp = make_inputs(w)
+    A, B, C = inp.A.cuda(), inp.B.cuda(), inp.C0.cuda()
+    G.gemm(A, B, C, w.alpha, w.beta, checked=True)
+    rows, cols = sample_indices(M, N, 1500, seed=11)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref, absb = oracle.gemm_entries(inp.A, inp.B, inp.C0, w.alpha, w.beta, rows=rows, cols=cols)
+    c0s = inp.C0[torch.from_numpy(rows), torch.from_numpy(cols)]
+    # The elementwise bound holds as stated.  The relative Frobenius bound
+    # (1e-4) is stated for K up to 8192; rounding in an fp32 accumulation
+    # grows like sqrt(K), so it is scaled by sqrt(K / 8192) beyond that.
+    check_against_oracle(got, ref, absb, GEMM_BF16_F32, beta=w.beta, C0=c0s,
+                         what=f"extreme {M}x{N}x{K}", frob=False)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 1e-4 * max(1.0, np.sqrt(K / 8192)), f"relative Frobenius error {rel:.3e}"
+
+
+def test_calls_replay_from_a_cuda_graph():
+    """gemm enqueues plain kernel launches (no allocation, no host sync on the
+    default schedule), so a sequence of calls can be captured into a CUDA
+    graph and replayed: three captured C += A*B, replayed twice, give
+    C0 + 6*A*B."""
+    w = workload(GEMM_BF16_F32, 700, 520, 264, beta=1.0)
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    C = inp.C0.cuda()
+    G.gemm(A, B, C.clone(), 1.0, 1.0)            # first call outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            G.gemm(A, B, C, 1.0, 1.0, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    ref, absb = oracle.gemm(inp.A, inp.B, inp.C0, 6.0, 1.0)
+    check_against_oracle(C.double().cpu().numpy(), ref, 6.0 * absb, GEMM_BF16_F32, beta=1.0,
+                         C0=inp.C0, what="graph replay")
 
 
 # --------------------------------------------------------------------------- stream-K tail
