@@ -505,6 +505,36 @@ def test_launch_goes_on_the_callers_stream():
                          C0=inp.C0, what="non-default stream")
 
 
+@pytest.mark.parametrize("schedule", [G.SCHEDULE_AUTO, G.SCHEDULE_STREAM_K])
+def test_concurrent_streams(schedule):
+    """Two GEMMs queued on two streams at once (their kernels may overlap on
+    the GPU) write their own C correctly; under stream-K each stream has its
+    own workspace."""
+    w1 = workload(GEMM_BF16_F32, 1100, 904, 2048, beta=1.0)
+    w2 = workload(GEMM_BF16_BF16, 700, 1000, 1504, beta=0.0)
+    in1, in2 = make_inputs(w1), make_inputs(w2)
+    A1, B1, C1 = in1.A.cuda(), in1.B.cuda(), in1.C0.cuda()
+    A2 = in2.A.cuda()
+    B2 = in2.B.t().contiguous().t().cuda() if w2.b_col_major else in2.B.cuda()
+    C2 = torch.zeros(700, 1000, dtype=torch.bfloat16, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    try:
+        G.schedule_set(schedule)
+        for _ in range(3):                      # C1 accumulates three products
+            G.gemm(A1, B1, C1, 1.0, 1.0, stream=s1)
+            G.gemm(A2, B2, C2, 1.0, 0.0, stream=s2)
+        torch.cuda.synchronize()
+    finally:
+        G.schedule_set(G.SCHEDULE_AUTO)
+    ref1, absb1 = oracle.gemm(in1.A, in1.B, in1.C0, 3.0, 1.0)
+    check_against_oracle(C1.double().cpu().numpy(), ref1, 3.0 * absb1, GEMM_BF16_F32, beta=1.0,
+                         C0=in1.C0, what=f"stream 1, schedule {schedule}")
+    ref2, absb2 = oracle.gemm(in2.A, in2.B, None, 1.0, 0.0)
+    check_against_oracle(C2.double().cpu().numpy(), ref2, absb2, GEMM_BF16_BF16,
+                         what=f"stream 2, schedule {schedule}")
+
+
 def test_release_then_reuse():
     G.load_library().gemm_host_release()
     inp = make_inputs(workload(GEMM_BF16_F32, 256, 256, 256, beta=0.0))
