@@ -331,6 +331,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    // The grid is launched with programmatic stream serialization: the next
+    // GEMM on the stream may be scheduled as soon as every CTA of this one has
+    // got here, so its CTAs take the SMs this grid's last round leaves idle
+    // and run their prologue early.  Nothing above touches global memory;
+    // nothing below does before the previous grid has completed.
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -903,20 +910,31 @@ bool smem_attribute(int dev, bool pair, int ka) {
     return done[dev][pair][ka - 1];
 }
 
-// Launch configuration: clusters of `cluster` CTAs (2 for the pair tile).
+// Launch configuration: clusters of `cluster` CTAs (2 for the pair tile),
+// and, for a real launch, programmatic stream serialization (see the kernel's
+// griddepcontrol).  attr must hold two entries.
 void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int cluster,
-                   size_t smem, cudaStream_t stream) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+                   size_t smem, cudaStream_t stream, bool programmatic) {
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (programmatic) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(grid);
     cfg->blockDim = dim3(NUM_THREADS);
     cfg->dynamicSmemBytes = smem;
     cfg->stream = stream;
     cfg->attrs = attr;
-    cfg->numAttrs = cluster > 1 ? 1 : 0;
+    cfg->numAttrs = static_cast<unsigned>(n);
 }
 
 // Number of CTA pairs that can be resident at once for a given shared-memory
@@ -930,8 +948,8 @@ int max_resident_pairs(int dev, size_t smem) {
     for (int i = 0; i < 8; ++i)
         if (key_smem[dev][i] == smem && val[dev][i] > 0) return val[dev][i];
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    launch_config(&cfg, attr, 2, 2, smem, nullptr);
+    cudaLaunchAttribute attr[2];
+    launch_config(&cfg, attr, 2, 2, smem, nullptr, false);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, 2), &cfg) != cudaSuccess) n = 0;
     for (int i = 0; i < 8; ++i)
@@ -1095,8 +1113,8 @@ bool encode_maps(const TcLaunch& L, int bks, bool chunked, CUtensorMap* tmA, CUt
 int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                   const CUtensorMap& tmC, const TcParams& p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    launch_config(&cfg, attr, geo.grid, geo.cluster, geo.smem, stream);
+    cudaLaunchAttribute attr[2];
+    launch_config(&cfg, attr, geo.grid, geo.cluster, geo.smem, stream, true);
     if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.ka), tmA, tmB, tmC, p) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;

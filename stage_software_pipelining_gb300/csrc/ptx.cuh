@@ -100,6 +100,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
 // 2-D tiled bulk tensor copy shared -> global (completion through the bulk
 // async-group of the issuing thread).  Parts of the box outside the tensor
 // are not written.
+// Programmatic dependent launch: let the next grid on the stream (launched
+// with programmatic stream serialization) start, and wait until the grids
+// this one depends on have completed and their memory is visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Add a shared-memory box into global memory element by element
 // (cp.reduce.async.bulk.tensor .add): the add happens at L2, so C is never
 // read into the SM.  For f32 it rounds to nearest once and keeps subnormals
