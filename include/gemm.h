@@ -81,8 +81,10 @@ typedef enum {
  * 128 columns of B per K step and holds 128 rows of the 256 x 256 result.
  * The stage limits are what fits in 227 KB of shared memory per CTA. */
 typedef enum {
-    GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128,
-                                    else 128x128 (N <= 128) or 128x256 */
+    GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128
+                                    (128x128 if the pair tiles would number at
+                                    most a quarter of the SMs), else 128x128
+                                    (N <= 128) or 128x256 */
     GEMM_TILE_128x128 = 128,     /* one CTA, K = 128 per stage, stages 1..3 (64 KB each) */
     GEMM_TILE_128x256 = 256,     /* one CTA, K = 64 per stage, stages 1..4 (48 KB each) */
     GEMM_TILE_256x256_2SM = 512  /* a CTA pair, K = 128 per stage, stages 1..3

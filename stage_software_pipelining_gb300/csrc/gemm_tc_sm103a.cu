@@ -1198,6 +1198,12 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
     return launch_kernel(geo, pair, tmA, tmB, tmC, p, stream);
 }
 
+int tc_current_device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return device_sms(dev);
+}
+
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes) {
     TcParams p;
     Geometry geo;

@@ -63,6 +63,9 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream);
 int tc_plan(const TcLaunch& L, int* grid, int* cluster, int* smem_bytes);
 // Free the stream-K workspaces of the current device.
 int tc_release_workspaces();
+
+// SM count of the current device (0 when it cannot be queried).
+int tc_current_device_sms();
 // Zero the stream-K flags of every workspace of the current device (after a
 // run that gave up; synchronous).
 int tc_clear_workspace_flags();
