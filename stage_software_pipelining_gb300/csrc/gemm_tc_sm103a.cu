@@ -19,7 +19,12 @@
 //   * the release is tcgen05.commit, which arrives on the stage's "empty"
 //     barrier once the MMAs reading it have finished;
 //   * the CTA is persistent and keeps two accumulators in TMEM, so the
-//     epilogue of one output tile overlaps the mainloop of the next.
+//     epilogue of one output tile overlaps the mainloop of the next;
+//   * a stage holds K = 128 (8 MMAs) so that the per-stage wait and commit
+//     stay off the tensor pipe's critical path;
+//   * the epilogue moves C with tensor copies (and, for beta = 1 with fp32 C,
+//     adds into C at L2 with tensor reduces), and consecutive GEMMs on a
+//     stream overlap their prologue through programmatic dependent launch.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)...).
@@ -28,9 +33,9 @@
 // handles): the producer waits empty[s] for parity (n&1)^1, arms full[s] with
 // the stage's byte count and issues the copies; the MMA thread waits full[s]
 // for parity n&1, issues the stage's MMAs (K = 64 * KA per stage, 16 per MMA)
-// and commits to empty[s].  With S = 1 the
-// producer's next copy waits for the MMAs of the same slot: the page's single
-// buffer with a load phase and a compute phase.
+// and commits to empty[s].  With S = 1 the producer's next copy waits for the
+// MMAs of the same slot: the page's single buffer with a load phase and a
+// compute phase.
 //
 // Every wait is bounded (wait_limit_ns, %globaltimer).  A wait that runs out
 // records the failure in g_gemm_status, raises a shared abort flag that the
