@@ -536,10 +536,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         volatile int* epi_ok = ctl->epi_ok;
         // Output boxes of 32 rows x 128 bytes: 32 fp32 or 64 bf16 columns.
         const int cw = p.out_bf16 ? 64 : 32;
-        // This warp's ring of nb output boxes (32 rows x 128 bytes, 4 KB):
-        // with beta != 0 each box is first filled with C by a tensor copy
-        // (issued up to nb boxes ahead, the first ones before the accumulator
-        // is ready), updated in place, then stored by a tensor copy.
+        // This warp's ring of nb output boxes (32 rows x 128 bytes, 4 KB),
+        // each written back by one tensor copy: a store, or for beta = 1 with
+        // fp32 C a reduce-add at L2.  For other beta != 0 the box is first
+        // filled with C by a tensor copy (issued up to nb boxes ahead, the
+        // first ones before the accumulator is ready) and updated in place.
         const int nb = p.epi_bufs;
         const uint32_t epi_buf0 = smem_addr(epi_ring) + static_cast<uint32_t>(q * nb) * 4096u;
         const uint32_t cbar0 = smem_addr(&ctl->cbar[q * kEpiMaxBufs]);
