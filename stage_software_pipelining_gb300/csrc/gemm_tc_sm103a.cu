@@ -976,10 +976,11 @@ struct Geometry {
     size_t ws_bytes = 0;  // stream-K workspace (partials + flags), 0 if unused
 };
 
-// Byte offset of the flags inside a workspace of `units` partial slots.
-size_t ws_flag_offset(int units, int ctas_per_unit, int bn) {
-    return static_cast<size_t>(units) * ctas_per_unit * BM * bn * sizeof(float);
-}
+// Stream-K workspace layout: the flags first (one per unit and CTA rank),
+// then one fp32 partial tile per unit and CTA.  The flags keep their place
+// whatever the tile, so a workspace that a call with another tile reuses
+// never has old partial data where this call's flags are.
+constexpr size_t kWsFlagBytes = 4096;  // room for 1024 flags
 
 // Stream-K workspaces, one per (device, stream): calls on one stream are
 // ordered, so they never share a workspace concurrently.
@@ -990,7 +991,7 @@ struct Workspace {
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
-int workspace_for(int dev, cudaStream_t stream, size_t bytes, size_t flag_off, void** out) {
+int workspace_for(int dev, cudaStream_t stream, size_t bytes, void** out) {
     std::lock_guard<std::mutex> g(g_ws_mu);
     Workspace& w = g_ws[{dev, stream}];
     if (w.bytes < bytes) {
@@ -1001,7 +1002,6 @@ int workspace_for(int dev, cudaStream_t stream, size_t bytes, size_t flag_off, v
         if (cudaMemset(w.ptr, 0, bytes) != cudaSuccess) return GEMM_ERR_CUDA;
         w.bytes = bytes;
     }
-    (void)flag_off;
     *out = w.ptr;
     return GEMM_OK;
 }
@@ -1091,7 +1091,7 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
         p.sk_iters = static_cast<long long>(sk_tiles) * KT;
         geo.units = U;
         const int cpu = pair ? 2 : 1;
-        geo.ws_bytes = ws_flag_offset(U, cpu, bn) + static_cast<size_t>(U) * cpu * sizeof(unsigned int);
+        geo.ws_bytes = kWsFlagBytes + static_cast<size_t>(U) * cpu * BM * bn * sizeof(float);
     } else {
         geo.units = T < U ? T : U;
     }
@@ -1130,7 +1130,6 @@ int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const 
 
 int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
-    const int bn = L.tile_n;
     TcParams p;
     Geometry geo;
     int st = plan(L, p, geo);
@@ -1141,11 +1140,10 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
         void* ws = nullptr;
-        const size_t flag_off = ws_flag_offset(geo.units, pair ? 2 : 1, bn);
-        st = workspace_for(dev, stream, geo.ws_bytes, flag_off, &ws);
+        st = workspace_for(dev, stream, geo.ws_bytes, &ws);
         if (st != GEMM_OK) return st;
-        p.ws = static_cast<float*>(ws);
-        p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
+        p.ws_flag = static_cast<unsigned int*>(ws);
+        p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsFlagBytes);
     }
     return launch_kernel(geo, pair, tmA, tmB, tmC, p, stream);
 }
@@ -1179,7 +1177,6 @@ int noalloc_scratch_address(int dev, void** out) {
 
 int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
     const bool pair = L.pair != 0;
-    const int bn = L.tile_n;
     TcParams p;
     Geometry geo;
     int st = plan(L, p, geo);
@@ -1193,13 +1190,10 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
         void* ws = nullptr;
         st = noalloc_scratch_address(dev, &ws);
         if (st != GEMM_OK) return st;
-        const size_t flag_off = ws_flag_offset(geo.units, pair ? 2 : 1, bn);
         // The array keeps the previous call's contents: the flags must start at 0.
-        if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + flag_off, 0, geo.ws_bytes - flag_off,
-                            stream) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        p.ws = static_cast<float*>(ws);
-        p.ws_flag = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + flag_off);
+        if (cudaMemsetAsync(ws, 0, kWsFlagBytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        p.ws_flag = static_cast<unsigned int*>(ws);
+        p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsFlagBytes);
     }
     return launch_kernel(geo, pair, tmA, tmB, tmC, p, stream);
 }

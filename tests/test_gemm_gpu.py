@@ -452,6 +452,18 @@ def test_stream_k_stage_invariance_and_beta(stream_k, tile):
                          what=f"stream-K beta=1 tile={tile}")
 
 
+def test_stream_k_workspace_reused_across_tiles(stream_k):
+    """One stream, one cached workspace, calls with tiles whose partial slots
+    differ in size, largest first: each call's flags must start cleared
+    wherever an earlier call left its partials."""
+    inp = make_inputs(workload(GEMM_BF16_F32, 768, 1280, 1024, beta=0.0))
+    ref, absb = oracle_full(inp)
+    for tile in (G.TILE_256x256_2SM, G.TILE_128x128, G.TILE_128x256, G.TILE_128x128,
+                 G.TILE_256x256_2SM):
+        out, _ = run_gpu(inp, 2, tile=tile)
+        check_against_oracle(out, ref, absb, GEMM_BF16_F32, what=f"stream-K reuse tile={tile}")
+
+
 def test_stream_k_schedules_agree_within_tolerance():
     inp = make_inputs(workload(GEMM_BF16_F32, 1024, 1536, 2048, beta=0.0))
     ref, absb = oracle_full(inp)
