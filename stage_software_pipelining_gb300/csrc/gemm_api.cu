@@ -315,8 +315,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
         if (cudaEventRecord(hp->in_done[pi], hp->in) != cudaSuccess ||
             cudaStreamWaitEvent(s, hp->in_done[pi], 0) != cudaSuccess)
             return fail();
+        // Every panel uses the tile chosen for the whole of M, so that the
+        // panels compute exactly what one call over all of M would.
         st = run(r1 - r0, N, K, need_ab ? pA : hA, lda, need_ab ? dB : B, ldb, pC, ldc, alpha,
-                 beta, dtype, stages, b_col_major, tile, s);
+                 beta, dtype, stages, b_col_major, is_tc(dtype) ? v.tile : tile, s);
         if (st != GEMM_OK) {
             fail();
             return st;

@@ -292,7 +292,9 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
     """Tall problems go through gemm_host in row panels (copies in, GEMM and
     copies back overlapped on three streams): every panel, including a
     ragged last one, gives the same bits as one device-side call."""
-    M, N, K = 2300, 520, 200
+    # 2300 rows: 5 panels of 512, the last of 252 rows, for which the automatic
+    # tile on its own would differ from the one chosen for the whole call
+    M, N, K = 2300, 1400, 200
     w = workload(dtype, M, N, K, beta=beta, b_col_major=(dtype == GEMM_BF16_BF16))
     inp = make_inputs(w)
     if inp.C0 is None:
@@ -300,6 +302,9 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
     out_dev, _ = run_gpu(inp, 2, beta=beta)
     Ch = inp.C0.clone().pin_memory()
     hB = inp.B.t().contiguous().pin_memory().t() if w.b_col_major else inp.B.pin_memory()
+    if dtype != GEMM_F32:     # the whole call takes the pair tile, a lone last panel would not
+        assert G.plan(M, N, K, dtype, 2, w.b_col_major)["cluster"] == 2
+        assert G.plan(252, N, K, dtype, 2, w.b_col_major)["cluster"] == 1
     G.gemm_host(inp.A.pin_memory(), hB, Ch, w.alpha, beta, stages=2)
     assert np.array_equal(Ch.double().numpy(), out_dev)
     ref, absb = oracle_full(inp, beta=beta)
