@@ -218,8 +218,7 @@ def run_ours(args):
     w = BY_NAME[args.workload]
     tile = args.tile
     if w.dtype != GEMM_F32 and tile == 0:
-        tile = G.TILE_256x256_2SM if (w.M > 128 and w.N > 128) else \
-            (G.TILE_128x128 if w.N <= 128 else G.TILE_128x256)
+        tile = G.resolve_tile(w.M, w.N, w.K, w.dtype)   # the library's automatic choice
     if w.dtype == GEMM_F32:
         stages = args.stages or 2
     else:

@@ -83,8 +83,10 @@ typedef enum {
 typedef enum {
     GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128
                                     (128x128 if the pair tiles would number at
-                                    most a quarter of the SMs), else 128x128
-                                    (N <= 128) or 128x256 */
+                                    most a quarter of the SMs, 128x256 if at
+                                    most half and K <= 4096), else 128x128
+                                    (N <= 128) or 128x256; gemm_resolve_tile
+                                    tells which */
     GEMM_TILE_128x128 = 128,     /* one CTA, K = 128 per stage, stages 1..3 (64 KB each) */
     GEMM_TILE_128x256 = 256,     /* one CTA, K = 64 per stage, stages 1..4 (48 KB each) */
     GEMM_TILE_256x256_2SM = 512  /* a CTA pair, K = 128 per stage, stages 1..3
@@ -179,6 +181,14 @@ const char* gemm_status_string(int status);
 /* Largest `stages` value accepted for a dtype and tile (as in gemm_ex), or
  * GEMM_ERR_ARG for an unknown combination. */
 int gemm_max_stages(int dtype, int tile);
+
+/*
+ * gemm_resolve_tile -- the gemm_tile_t that gemm_ex uses for these sizes on
+ * the current device when passed `tile` (GEMM_TILE_AUTO resolves to a tile
+ * code; an explicit tile comes back unchanged).  GEMM_ERR_ARG for a dtype
+ * of the SIMT path, a negative size or an unknown tile code.
+ */
+int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile);
 
 /*
  * gemm_plan -- the launch gemm_ex would make for these sizes, without making

@@ -26,16 +26,22 @@ int out_size(int dtype) { return dtype == GEMM_BF16_BF16 ? 2 : 4; }
 
 // Tensor-core tile for a request (0 = invalid tile code).  The default is the
 // 256 x 256 tile on a CTA pair unless M or N is a single 128-wide tile, or
-// the pair tiles would keep fewer than a quarter of the SMs busy: then
-// 128 x 128 tiles (four per pair tile, each on one SM) still fit in one round
-// and finish in about half the time (1024^2 x 4096: 459 vs 316 TFLOP/s).
-int resolve_tile(int64_t M, int64_t N, int tile) {
+// the pair tiles make one partial round (measured on GB300, bf16):
+//   * at most a quarter of the SMs busy: 128 x 128 tiles (four per pair
+//     tile, one SM each) still fit in one round and finish in about half the
+//     time (1024^2 x 4096: 459 vs 316 TFLOP/s);
+//   * at most half of them busy and K <= 4096: the one-CTA 128 x 256 tile
+//     (the same work per SM in the same single round) runs 4-9 % faster
+//     (2048^2 x 1024 / 2048 / 4096); at K = 8192 the pair stays ahead.
+int resolve_tile(int64_t M, int64_t N, int64_t K, int tile) {
     if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM)
         return tile;
     if (tile != GEMM_TILE_AUTO) return 0;
     if (M > 128 && N > 128) {
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        if (pair_tiles * 4 <= ssp::tc_current_device_sms()) return GEMM_TILE_128x128;
+        const int sms = ssp::tc_current_device_sms();
+        if (pair_tiles * 4 <= sms) return GEMM_TILE_128x128;
+        if (pair_tiles * 2 <= sms && K <= 4096) return GEMM_TILE_128x256;
         return GEMM_TILE_256x256_2SM;
     }
     return N <= 128 ? GEMM_TILE_128x128 : GEMM_TILE_128x256;
@@ -74,7 +80,7 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, c
     if (M < 0 || N < 0 || K < 0) return {GEMM_ERR_ARG, 0};
     if (b_col_major != 0 && b_col_major != 1) return {GEMM_ERR_ARG, 0};
     if (is_tc(dtype)) {
-        r.tile = resolve_tile(M, N, tile);
+        r.tile = resolve_tile(M, N, K, tile);
         if (r.tile == 0) return {GEMM_ERR_ARG, 0};
         if (stages < 1 || stages > ssp::kTcMaxStages) return {GEMM_ERR_ARG, 0};
         if (stages > tile_max_stages(r.tile)) return {GEMM_ERR_UNSUPPORTED, 0};
@@ -376,6 +382,12 @@ int gemm_max_stages(int dtype, int tile) {
     if (tile == GEMM_TILE_AUTO) return ssp::kTcMaxStages;
     const int m = tile_max_stages(tile);
     return m > 0 ? m : GEMM_ERR_ARG;
+}
+
+int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile) {
+    if (!is_tc(dtype) || M < 0 || N < 0 || K < 0) return GEMM_ERR_ARG;
+    const int t = resolve_tile(M, N, K, tile);
+    return t != 0 ? t : GEMM_ERR_ARG;
 }
 
 int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_major, int tile,

@@ -39,6 +39,7 @@ SIMT_FRAGMENTS_SINGLE = 1
 # Every extern "C" symbol include/gemm.h declares.
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
            "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
+           "gemm_resolve_tile",
            "pipelined_copy", "gemm_schedule_set", "gemm_noalloc")
 
 _lock = threading.Lock()
@@ -79,6 +80,8 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_max_stages.argtypes = [i32, i32]
         lib.gemm_debug_set.argtypes = [i64, i32]
         lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p, p, p]
+        lib.gemm_resolve_tile.argtypes = [i64, i64, i64, i32, i32]
+        lib.gemm_resolve_tile.restype = i32
         lib.pipelined_copy.argtypes = [p, p, i64, i32, p]
         lib.pipelined_copy.restype = i32
         lib.gemm_schedule_set.argtypes = [i32]
@@ -209,6 +212,14 @@ def raw_call(name: str, *args) -> int:
 
 def max_stages(dtype: int, tile: int = TILE_AUTO) -> int:
     return int(load_library().gemm_max_stages(int(dtype), int(tile)))
+
+
+def resolve_tile(M: int, N: int, K: int, dtype: int, tile: int = TILE_AUTO) -> int:
+    """The TILE_* code gemm uses for these sizes on the current device."""
+    t = int(load_library().gemm_resolve_tile(M, N, K, int(dtype), int(tile)))
+    if t < 0:
+        raise GemmError(t, "gemm_resolve_tile")
+    return t
 
 
 def plan(M: int, N: int, K: int, dtype: int, stages: int, b_col_major: bool = False,

@@ -132,6 +132,19 @@ def test_status_strings(lib):
     assert "unknown" in lib.gemm_status_string(42).decode()
 
 
+def test_resolve_tile_without_a_device(lib):
+    """Explicit tiles come back unchanged; SIMT types and bad codes are
+    refused; on a host without a GPU the automatic choice is the pair tile
+    for large M and N and the one-CTA tiles for a single 128-row/column."""
+    for t in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM):
+        assert lib.gemm_resolve_tile(4096, 4096, 4096, GEMM_BF16_F32, t) == t
+    assert lib.gemm_resolve_tile(8, 8, 8, GEMM_F32, 0) == G.GEMM_ERR_ARG
+    assert lib.gemm_resolve_tile(8, 8, 8, GEMM_BF16_F32, 192) == G.GEMM_ERR_ARG
+    assert lib.gemm_resolve_tile(-1, 8, 8, GEMM_BF16_F32, 0) == G.GEMM_ERR_ARG
+    assert lib.gemm_resolve_tile(100, 4096, 64, GEMM_BF16_F32, 0) == G.TILE_128x256
+    assert lib.gemm_resolve_tile(4096, 100, 64, GEMM_BF16_F32, 0) == G.TILE_128x128
+
+
 def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_F32, 0) == 4
     assert lib.gemm_max_stages(GEMM_F32, 1) == 4      # single register fragment set

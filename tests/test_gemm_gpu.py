@@ -246,6 +246,20 @@ def G_in(dtype):
     return IN_DTYPE[dtype]
 
 
+def test_automatic_tile_choice_on_gb300():
+    """The automatic tile on this GPU: the pair tile once the pair tiles fill
+    more than half the SMs (or K is long), 128 x 256 for one partial round at
+    K <= 4096, 128 x 128 when the pair tiles would busy at most a quarter."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sms >= 128
+    dt = GEMM_BF16_F32
+    assert G.resolve_tile(8192, 8192, 8192, dt) == G.TILE_256x256_2SM
+    assert G.resolve_tile(2048, 2048, 2048, dt) == G.TILE_128x256     # 64 pair tiles
+    assert G.resolve_tile(2048, 2048, 8192, dt) == G.TILE_256x256_2SM
+    assert G.resolve_tile(1024, 1024, 4096, dt) == G.TILE_128x128     # 16 pair tiles
+    assert G.resolve_tile(8191, 28672, 4096, GEMM_BF16_BF16) == G.TILE_256x256_2SM
+
+
 def test_empty_m_or_n_is_a_noop():
     C = torch.full((0, 16), 1.0, device="cuda")
     G.gemm(torch.zeros(0, 8, dtype=torch.bfloat16, device="cuda"),
@@ -294,7 +308,7 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
     ragged last one, gives the same bits as one device-side call."""
     # 2300 rows: 5 panels of 512, the last of 252 rows, for which the automatic
     # tile on its own would differ from the one chosen for the whole call
-    M, N, K = 2300, 1400, 200
+    M, N, K = 2300, 2304, 200
     w = workload(dtype, M, N, K, beta=beta, b_col_major=(dtype == GEMM_BF16_BF16))
     inp = make_inputs(w)
     if inp.C0 is None:
