@@ -155,7 +155,7 @@ int gemm_checked(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
  * gemm_host -- the same operation on HOST buffers: copies A, B (and C when
  * beta != 0) to the device, runs gemm_ex, copies C back and synchronises.
  * The copies are pipelined with the computation: B goes first, then M is cut
- * into up to 8 row panels (whole 256-row tiles); panel p's rows of A and C
+ * into up to 16 row panels (whole 256-row tiles); panel p's rows of A and C
  * are copied in on an internal stream while panel p-1 is computed on
  * `stream` and earlier panels' C rows are copied back on a second internal
  * stream.  Every panel gives the same bits as one gemm_ex over all of M.

@@ -162,7 +162,7 @@ std::mutex g_staging_mu;
 Staging g_staging[64];
 
 // gemm_host's copy streams and events, created on first use per device.
-constexpr int kHostPanels = 8;  // row panels a large gemm_host call is cut into
+constexpr int kHostPanels = 16;  // row panels a large gemm_host call is cut into
 struct HostPipe {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;  // host->device and device->host copies

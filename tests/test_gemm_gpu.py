@@ -306,7 +306,7 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
     """Tall problems go through gemm_host in row panels (copies in, GEMM and
     copies back overlapped on three streams): every panel, including a
     ragged last one, gives the same bits as one device-side call."""
-    # 2300 rows: 5 panels of 512, the last of 252 rows, for which the automatic
+    # 2300 rows: 9 panels of 256, the last of 252 rows, for which the automatic
     # tile on its own would differ from the one chosen for the whole call
     M, N, K = 2300, 2304, 200
     w = workload(dtype, M, N, K, beta=beta, b_col_major=(dtype == GEMM_BF16_BF16))
