@@ -248,6 +248,10 @@ def run_ours(args):
     sampler = ClockSampler(phys)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # The tensor-core kernel's own SM clock: CTA 0 of each timed launch adds
+    # its clock ticks and nanoseconds here (two atomics per launch).
+    clk_log = torch.zeros(2, dtype=torch.int64, device=dev)
+    G.clock_log(clk_log)
     sampler.start()
     barrier()
     t0.record(stream)
@@ -259,6 +263,9 @@ def run_ours(args):
     t1.record(stream)
     barrier()
     clocks = sampler.stop()
+    G.clock_log(None)
+    ticks, ns = (int(v) for v in clk_log.tolist())
+    kernel_mhz = ticks * 1000.0 / ns if ns > 0 else None
     elapsed_ms = t0.elapsed_time(t1)
     launch_ms = elapsed_ms / args.steps
     elapsed_ms = rank_max(elapsed_ms, dev)
@@ -345,6 +352,22 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": flops_step,
                 "algorithmic_bytes_per_launch": algorithmic_bytes(w),
                 "kernel": "gemm_tc_kernel", "mean_launch_ms": round(launch_ms, 4)}
+        # The per-SM tensor rate measured on this GPU (after the timed region):
+        # the GEMM against SMs x that rate x the clock sampled under load.
+        rate = G.mma_rate(n_mma=8192)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        per_clock = {"flop_per_clk_per_sm": round(rate["flop_per_clk_per_sm"], 1),
+                     "probe": f"{rate['ctas']} CTAs x {rate['n_mma']} tcgen05.mma 128x256x16, "
+                              f"SM clocks per CTA {rate['cycles_min']}..{rate['cycles_max']}",
+                     "peak_at_max_clock": round(rate["flop_per_clk_per_sm"] * sms
+                                                * peaks.get("sm_max_mhz", 2070.0) * 1e-6, 1)}
+        if kernel_mhz:
+            # the clock the GEMM itself ran at (CTA 0's clock64 over globaltimer)
+            pk = rate["flop_per_clk_per_sm"] * sms * kernel_mhz * 1e-6
+            per_clock.update({"kernel_sm_mhz": round(kernel_mhz, 1),
+                              "peak_at_kernel_clock": round(pk, 1),
+                              "frac": round(achieved / pk, 4)})
+        roof["per_clock"] = per_clock
 
     cpu = None
     if rank == 0 and not args.no_cpu:

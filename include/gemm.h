@@ -273,6 +273,28 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void* stream);
 
 /*
+ * mma_rate -- the tensor pipe's dense bf16 rate on this GPU, in SM clocks:
+ * the per-SM factor of the GEMM's compute roofline (SMs x FLOP per SM per
+ * clock x clock), measured rather than taken from a data sheet.
+ *
+ * `ctas` CTAs (at most one per SM) each fill a 128 x 64 and a 256 x 64 bf16
+ * operand tile in shared memory, then issue n_mma back-to-back tcgen05.mma
+ * (cta_group::1, kind::f16, M = 128, N = 256, K = 16, fp32 accumulate in
+ * TMEM) from one thread; no global memory is read in between.  Each CTA reads
+ * its SM clock (clock64) before the first issue and after the commit of the
+ * last MMA has arrived.  FLOP per SM per clock = n_mma * 2*128*256*16 /
+ * cycles[i].
+ *   n_mma        1 .. 2^20 MMAs per CTA (GEMM_ERR_ARG otherwise)
+ *   ctas         1 .. the device's SM count (GEMM_ERR_ARG otherwise)
+ *   cycles       host array of `ctas` entries, written: SM clocks per CTA
+ *   elapsed_ms   host pointer, written: CUDA-event time of the launch
+ * Runs on the current device's legacy default stream and returns when the
+ * kernel has finished (synchronous).  A CTA whose wait for its MMAs runs out
+ * (2 s) writes -1 and the call returns GEMM_ERR_TIMEOUT.
+ */
+int mma_rate(int n_mma, int ctas, long long* cycles, float* elapsed_ms);
+
+/*
  * gemm_debug_set -- test hook for the bounded waits (not thread-safe; affects
  * later launches of the tensor-core kernel from this process).
  *   wait_limit_ns      time a pipeline wait may spin before it gives up
@@ -284,6 +306,19 @@ int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void
  *                      instead of a hang.
  */
 int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive);
+
+/*
+ * gemm_clock_log -- measurement hook (not thread-safe; affects later launches
+ * of the tensor-core kernel from this process).  With dev_buf non-null, CTA 0
+ * of every later launch adds, when it exits, its SM clock ticks (clock64) to
+ * dev_buf[0] and its wall-clock nanoseconds (globaltimer) to dev_buf[1],
+ * both counted from the point where it may first touch global memory.
+ * dev_buf[0] * 1000 / dev_buf[1] is then the launches' mean SM clock in MHz.
+ *   dev_buf   device pointer to two zeroed 64-bit unsigned integers, owned by
+ *             the caller, live until every launch made while it was set has
+ *             finished; NULL turns the hook off (the default)
+ */
+int gemm_clock_log(void* dev_buf);
 
 #ifdef __cplusplus
 }

@@ -15,6 +15,7 @@ namespace {
 
 int64_t g_wait_limit_ns = 2000000000LL;  // 2 s per pipeline wait
 int g_withhold_arrive = -1;
+unsigned long long* g_clock_log = nullptr;  // gemm_clock_log
 int g_schedule = 0;  // tensor-core tile schedule (gemm_schedule_set)
 
 bool is_tc(int dtype) {
@@ -130,6 +131,7 @@ ssp::TcLaunch tc_request(int64_t M, int64_t N, int64_t K, const void* A, int64_t
     L.pair = tile == GEMM_TILE_256x256_2SM;
     L.wait_limit_ns = g_wait_limit_ns;
     L.withhold_arrive = g_withhold_arrive;
+    L.clock_log = g_clock_log;
     L.schedule = g_schedule;
     return L;
 }
@@ -456,6 +458,11 @@ int gemm_schedule_set(int schedule) {
 int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive) {
     g_wait_limit_ns = wait_limit_ns > 0 ? wait_limit_ns : 2000000000LL;
     g_withhold_arrive = withhold_arrive < 0 ? -1 : withhold_arrive;
+    return GEMM_OK;
+}
+
+int gemm_clock_log(void* dev_buf) {
+    g_clock_log = static_cast<unsigned long long*>(dev_buf);
     return GEMM_OK;
 }
 

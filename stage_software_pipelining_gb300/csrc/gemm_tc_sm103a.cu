@@ -92,6 +92,7 @@ struct TcParams {
     long long sk_iters;
     int epi_bufs;           // output boxes per epilogue warp (2..kEpiMaxBufs)
     float* ws;              // one partial tile per unit (per CTA: 128 x bn fp32)
+    unsigned long long* clock_log;  // null, or [2]: CTA 0 adds its SM clocks and ns
     unsigned int* ws_flag;  // per unit and CTA rank: 1 = partial published
 };
 
@@ -343,6 +344,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // nothing below does before the previous grid has completed.
     griddep_launch_dependents();
     griddep_wait();
+    // SM clock of this launch (measurement hook): CTA 0's clock ticks and
+    // wall-clock nanoseconds from here to its exit.
+    const bool log_clock = p.clock_log != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+    long long clk0 = 0;
+    unsigned long long ns0 = 0;
+    if (log_clock) {
+        clk0 = clock64();
+        ns0 = globaltimer_ns();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -806,6 +816,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (PAIR) tmem_dealloc_pair(tmem_base, tmem_cols);
         else tmem_dealloc(tmem_base, tmem_cols);
     }
+    if (log_clock) {
+        atomicAdd(p.clock_log, static_cast<unsigned long long>(clock64() - clk0));
+        atomicAdd(p.clock_log + 1, globaltimer_ns() - ns0);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1043,6 +1057,7 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.ldc = L.ldc;
     p.wait_limit_ns = static_cast<unsigned long long>(L.wait_limit_ns);
     p.withhold = L.withhold_arrive;
+    p.clock_log = L.clock_log;
     p.dp_tiles = p.num_tiles;
     p.sk_iters = 0;
     p.ws = nullptr;

@@ -33,6 +33,7 @@ struct TcLaunch {
     int schedule;     // 0 auto, 1 full tiles only, 2 stream-K tail whenever a round is partial
     int64_t wait_limit_ns;
     int withhold_arrive;
+    unsigned long long* clock_log;  // device [2] or null: CTA 0's SM clocks and ns
 };
 
 struct SimtLaunch {

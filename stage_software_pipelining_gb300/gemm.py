@@ -40,7 +40,8 @@ SIMT_FRAGMENTS_SINGLE = 1
 EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
            "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
            "gemm_resolve_tile",
-           "pipelined_copy", "gemm_schedule_set", "gemm_noalloc")
+           "pipelined_copy", "gemm_schedule_set", "gemm_noalloc", "mma_rate",
+           "gemm_clock_log")
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +87,10 @@ def load_library(path: str = LIB_PATH):
         lib.pipelined_copy.restype = i32
         lib.gemm_schedule_set.argtypes = [i32]
         lib.gemm_schedule_set.restype = i32
+        lib.mma_rate.argtypes = [i32, i32, p, p]
+        lib.mma_rate.restype = i32
+        lib.gemm_clock_log.argtypes = [p]
+        lib.gemm_clock_log.restype = i32
         if path == LIB_PATH:
             _lib = lib
         return lib
@@ -250,6 +255,42 @@ def pipelined_copy(dst: torch.Tensor, src: torch.Tensor, stages: int = 2,
     if st != GEMM_OK:
         raise GemmError(st, "pipelined_copy")
     return dst
+
+
+# FLOPs of one tcgen05.mma of the rate probe: M = 128, N = 256, K = 16.
+MMA_RATE_FLOPS = 2 * 128 * 256 * 16
+
+
+def mma_rate(n_mma: int = 8192, ctas: int | None = None, device: int | None = None) -> dict:
+    """Dense bf16 tensor-pipe rate in FLOP per SM per clock (libgemm.so
+    mma_rate): `ctas` CTAs (default: one per SM) each issue n_mma
+    back-to-back 128 x 256 x 16 MMAs and count SM clocks.  Synchronous."""
+    dev = torch.cuda.current_device() if device is None else int(device)
+    if ctas is None:
+        ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = (ctypes.c_longlong * int(ctas))()
+    ms = ctypes.c_float()
+    with torch.cuda.device(dev):
+        st = load_library().mma_rate(int(n_mma), int(ctas), cycles, ctypes.byref(ms))
+    if st != GEMM_OK:
+        raise GemmError(st, "mma_rate")
+    cyc = sorted(int(c) for c in cycles)
+    flops = n_mma * MMA_RATE_FLOPS
+    return {"n_mma": int(n_mma), "ctas": int(ctas),
+            "cycles_min": cyc[0], "cycles_median": cyc[len(cyc) // 2], "cycles_max": cyc[-1],
+            "flop_per_clk_per_sm": flops / cyc[len(cyc) // 2],
+            "elapsed_ms": ms.value,
+            "tflops": flops * ctas / (ms.value * 1e-3) / 1e12}
+
+
+def clock_log(buf: torch.Tensor | None) -> None:
+    """Measurement hook (libgemm.so gemm_clock_log): with `buf` (two zeroed
+    int64 on the GPU), CTA 0 of every later tensor-core launch adds its SM
+    clock ticks to buf[0] and its nanoseconds to buf[1]; None turns it off."""
+    if buf is not None and (buf.device.type != "cuda" or buf.dtype != torch.int64
+                            or buf.numel() < 2 or not buf.is_contiguous()):
+        raise ValueError("clock_log takes two contiguous int64 on the GPU")
+    load_library().gemm_clock_log(None if buf is None else buf.data_ptr())
 
 
 SCHEDULE_AUTO, SCHEDULE_FULL_TILES, SCHEDULE_STREAM_K = 0, 1, 2

@@ -221,3 +221,23 @@ def test_noalloc_entry_validates_on_the_host(lib):
               None) == G.GEMM_ERR_UNSUPPORTED
     assert na(0, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0, None) == G.GEMM_OK
     assert "fixed array" in lib.gemm_status_string(G.GEMM_ERR_SCRATCH).decode()
+
+
+def test_mma_rate_argument_checks(lib):
+    cyc = (ctypes.c_longlong * 4)()
+    ms = ctypes.c_float()
+    # answered before any CUDA call
+    assert lib.mma_rate(0, 4, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate((1 << 20) + 1, 4, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate(16, 0, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate(16, 4, None, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate(16, 4, cyc, None) == G.GEMM_ERR_ARG
+
+
+def test_cublas_comparison_entry_parses_without_a_gpu():
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-m", "stage_software_pipelining_gb300.vs_cublas", "--help"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "--launches" in r.stdout
