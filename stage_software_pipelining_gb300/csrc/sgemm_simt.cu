@@ -17,6 +17,15 @@
 // one barrier per iteration, as the pages' double-buffered loops have.
 // Out-of-range rows/columns are zero-filled by cp.async's source-size operand,
 // so ragged M, N and K need no special path; stores are masked.
+//
+// GB300 form of the outer product: the 64 multiply-adds of a k step are 32
+// packed fp32 FMAs (fma.rn.f32x2, sm_100 and later).  Each lane of one is an
+// ordinary fused multiply-add rounded once to nearest, so C is bit-for-bit
+// what 64 scalar fmaf would give; the packed form halves the issue slots the
+// FMAs take, which is what limits a register-blocked sgemm.  A thread keeps
+// its 8 x 8 accumulators as 8 x 4 pairs of adjacent columns, reads its B
+// fragment from shared memory directly as such pairs, and duplicates each A
+// value into both halves of a pair.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -82,13 +91,33 @@ __device__ __forceinline__ void load_tile(const SimtParams& p, int m0, int n0, i
     }
 }
 
-// acc[r][j] += A[ty + 16 r][k] * B[k][col(j)] over the BK values of one stage.
+// Two fp32 in one 64-bit register: the low half is the even column.
+using Pair = unsigned long long;
+
+__device__ __forceinline__ Pair dup2(float x) {
+    Pair r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+
+// c.lo = fma(a.lo, b.lo, c.lo); c.hi = fma(a.hi, b.hi, c.hi), each rounded once.
+__device__ __forceinline__ void ffma2(Pair& c, Pair a, Pair b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float lo32(Pair v) { return __uint_as_float(static_cast<unsigned>(v)); }
+__device__ __forceinline__ float hi32(Pair v) {
+    return __uint_as_float(static_cast<unsigned>(v >> 32));
+}
+
+// acc[r][q] += A[ty + 16 r][k] * B[k][cols of pair q] over the BK values of one
+// stage (pair q: columns 4tx+2q, +1 for q < 2, 32+4tx+2(q-2), +1 for q >= 2).
 // Thread rows are ty, ty+16, ..., ty+112; thread columns are 4tx..4tx+3 and
 // 32+4tx..32+4tx+3, so a warp's fragment reads hit distinct banks.
 // One fragment set: the A fragments of 4 consecutive k (8 float4) and the B
 // fragment of one k (2 float4) are loaded, then used.
 __device__ __forceinline__ void compute_tile_single(const float* As, const float* Bs, int ty,
-                                                    int tx, float (&acc)[8][8]) {
+                                                    int tx, Pair (&acc)[8][4]) {
 #pragma unroll
     for (int kq = 0; kq < BK; kq += 4) {
         float4 a4[8];
@@ -97,14 +126,16 @@ __device__ __forceinline__ void compute_tile_single(const float* As, const float
             a4[r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD + kq);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const float4 b0 = *reinterpret_cast<const float4*>(Bs + (kq + kk) * BN + 4 * tx);
-            const float4 b1 = *reinterpret_cast<const float4*>(Bs + (kq + kk) * BN + 32 + 4 * tx);
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(Bs + (kq + kk) * BN + 4 * tx);
+            const ulonglong2 b1 =
+                *reinterpret_cast<const ulonglong2*>(Bs + (kq + kk) * BN + 32 + 4 * tx);
+            const Pair b[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const float a = kk == 0 ? a4[r].x : kk == 1 ? a4[r].y : kk == 2 ? a4[r].z : a4[r].w;
+                const Pair a2 = dup2(a);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(a, b[j], acc[r][j]);
+                for (int q = 0; q < 4; ++q) ffma2(acc[r][q], a2, b[q]);
             }
         }
     }
@@ -116,14 +147,14 @@ __device__ __forceinline__ void compute_tile_single(const float* As, const float
 // step k+1 and, at the first step of each group of 4, the A fragments of the
 // next group are already being fetched from shared memory.
 __device__ __forceinline__ void compute_tile_double(const float* As, const float* Bs, int ty,
-                                                    int tx, float (&acc)[8][8]) {
+                                                    int tx, Pair (&acc)[8][4]) {
     float4 a4[2][8];
-    float4 bf[2][2];
+    ulonglong2 bf[2][2];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
         a4[0][r] = *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD);
-    bf[0][0] = *reinterpret_cast<const float4*>(Bs + 4 * tx);
-    bf[0][1] = *reinterpret_cast<const float4*>(Bs + 32 + 4 * tx);
+    bf[0][0] = *reinterpret_cast<const ulonglong2*>(Bs + 4 * tx);
+    bf[0][1] = *reinterpret_cast<const ulonglong2*>(Bs + 32 + 4 * tx);
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
         const int kq = k >> 2, kk = k & 3;
@@ -134,24 +165,25 @@ __device__ __forceinline__ void compute_tile_double(const float* As, const float
                     *reinterpret_cast<const float4*>(As + (ty + 16 * r) * A_LD + k + 4);
         }
         if (k + 1 < BK) {
-            bf[(k + 1) & 1][0] = *reinterpret_cast<const float4*>(Bs + (k + 1) * BN + 4 * tx);
-            bf[(k + 1) & 1][1] = *reinterpret_cast<const float4*>(Bs + (k + 1) * BN + 32 + 4 * tx);
+            bf[(k + 1) & 1][0] = *reinterpret_cast<const ulonglong2*>(Bs + (k + 1) * BN + 4 * tx);
+            bf[(k + 1) & 1][1] =
+                *reinterpret_cast<const ulonglong2*>(Bs + (k + 1) * BN + 32 + 4 * tx);
         }
-        const float4 b0 = bf[k & 1][0], b1 = bf[k & 1][1];
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const Pair b[4] = {bf[k & 1][0].x, bf[k & 1][0].y, bf[k & 1][1].x, bf[k & 1][1].y};
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
             const float4 av = a4[kq & 1][r];
             const float a = kk == 0 ? av.x : kk == 1 ? av.y : kk == 2 ? av.z : av.w;
+            const Pair a2 = dup2(a);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(a, b[j], acc[r][j]);
+            for (int q = 0; q < 4; ++q) ffma2(acc[r][q], a2, b[q]);
         }
     }
 }
 
 template <bool FRAG_DB>
 __device__ __forceinline__ void compute_tile(const float* As, const float* Bs, int ty, int tx,
-                                             float (&acc)[8][8]) {
+                                             Pair (&acc)[8][4]) {
     if constexpr (FRAG_DB) compute_tile_double(As, Bs, ty, tx, acc);
     else compute_tile_single(As, Bs, ty, tx, acc);
 }
@@ -166,11 +198,11 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
     const int KT = (p.K + BK - 1) / BK;
 
-    float acc[8][8];
+    Pair acc[8][4];  // acc[r][q]: columns 2q, 2q+1 of the thread's 8 (bits of +0.0f: zero)
 #pragma unroll
     for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[r][j] = 0.0f;
+        for (int q = 0; q < 4; ++q) acc[r][q] = 0ull;
 
     if constexpr (STAGES == 1) {
         for (int kt = 0; kt < KT; ++kt) {
@@ -213,7 +245,10 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
             const int gn = n0 + 32 * h + 4 * tx;
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = p.alpha * acc[r][4 * h + j];
+            for (int j = 0; j < 4; ++j) {
+                const Pair pr = acc[r][2 * h + (j >> 1)];
+                v[j] = p.alpha * ((j & 1) ? hi32(pr) : lo32(pr));
+            }
             if (gn + 4 <= p.N) {
                 float4* cp = reinterpret_cast<float4*>(crow + gn);
                 if (p.beta != 0.0f) {
