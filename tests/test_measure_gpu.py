@@ -45,7 +45,8 @@ def test_rejects_more_ctas_than_sms():
         G.mma_rate(n_mma=16, ctas=sms + 1)
 
 
-def test_clock_log_of_the_gemm():
+@pytest.mark.parametrize("tile", [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM])
+def test_clock_log_of_the_gemm(tile):
     gen = torch.Generator().manual_seed(7)
     A = (torch.rand(2048, 2048, generator=gen) - 0.5).to(torch.bfloat16).cuda()
     B = (torch.rand(2048, 2048, generator=gen) - 0.5).to(torch.bfloat16).cuda()
@@ -54,7 +55,7 @@ def test_clock_log_of_the_gemm():
     G.clock_log(log)
     try:
         for _ in range(5):
-            G.gemm(A, B, C, 1.0, 0.0, stages=3)
+            G.gemm(A, B, C, 1.0, 0.0, stages=3, tile=tile)
         torch.cuda.synchronize()
     finally:
         G.clock_log(None)
@@ -63,7 +64,7 @@ def test_clock_log_of_the_gemm():
     mhz = ticks * 1000.0 / ns
     assert 300.0 <= mhz <= 2200.0, mhz
     # off: later launches add nothing
-    G.gemm(A, B, C, 1.0, 0.0, stages=3)
+    G.gemm(A, B, C, 1.0, 0.0, stages=3, tile=tile)
     torch.cuda.synchronize()
     assert log.tolist() == [ticks, ns]
     with pytest.raises(ValueError):
