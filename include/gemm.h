@@ -1,7 +1,8 @@
 /*
  * gemm.h -- C ABI of libgemm.so, the GB300 (sm_103a) software-pipelined GEMM.
  *
- * Operation (every entry point below):
+ * Operation (every gemm* entry point below; pipelined_copy, mma_rate and
+ * the hooks document their own):
  *
  *     C = alpha * A * B + beta * C
  *
