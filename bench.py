@@ -103,11 +103,12 @@ def kernel_hash() -> str:
 
 
 TILE_NAMES = {128: "128x128x128 (1 SM)", 256: "128x256x64 (1 SM)",
-              512: "256x256x128 (CTA pair, cta_group::2)"}
-TILE_MAX_STAGES = {128: 3, 256: 4, 512: 3}
+              512: "256x256x128 (CTA pair, cta_group::2)",
+              1024: "256x512x64 (CTA pair, cta_group::2, two N=256 MMAs per K step)"}
+TILE_MAX_STAGES = {128: 3, 256: 4, 512: 3, 1024: 4}
 SCHEDULE_NAMES = {0: "automatic", 1: "whole tiles", 2: "stream-K tail"}
 # Default ring depth per tile: the deepest ring that fits.
-TILE_DEFAULT_STAGES = {128: 3, 256: 4, 512: 3}
+TILE_DEFAULT_STAGES = {128: 3, 256: 4, 512: 3, 1024: 4}
 
 
 def committed_traffic(workload: str, stages: int, tile: int):
@@ -275,7 +276,7 @@ def run_ours(args):
     # the stage sweep (same workload, same launch stream)
     sweep = []
     if not args.no_sweep and w.dtype != GEMM_F32:
-        for tn in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM):
+        for tn in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM):
             for s in range(1, TILE_MAX_STAGES[tn] + 1):
                 reps = max(10, min(200, args.steps // 10))
                 for _ in range(3):

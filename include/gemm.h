@@ -19,8 +19,9 @@
  * a load phase and a compute phase per K tile, stages = 2 is double
  * buffering, stages >= 3 is a multi-stage ring.  The stage count changes
  * timing only: for one dtype and tile, every stage count gives bit-identical C.
- * A tensor-core stage holds a K slice of 128 (of 64 for the 128 x 256 tile)
- * of both operands: 8 (4) tcgen05.mma instructions per ring wait.
+ * A tensor-core stage holds a K slice of 128 (of 64 for the 128 x 256 and
+ * 256 x 512 tiles) of both operands: 8 tcgen05.mma instructions per ring wait
+ * (4 on the 128 x 256 tile).
  *
  * Layout (all row-major, leading dimensions in elements):
  *   A  M x K, element (i,k) at A[i*lda + k], lda >= K
@@ -77,21 +78,30 @@ typedef enum {
     GEMM_BF16_BF16 = 3
 } gemm_dtype_t;
 
-/* Tensor-core tile (gemm_ex's `tile`).  The 2-SM tile runs on a cluster of
+/* Tensor-core tile (gemm_ex's `tile`).  The 2-SM tiles run on a cluster of
  * two CTAs with tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and
- * 128 columns of B per K step and holds 128 rows of the 256 x 256 result.
+ * 128 (256 on the 512-wide tile) columns of B per K step and holds 128 rows
+ * of the result.
  * The stage limits are what fits in 227 KB of shared memory per CTA. */
 typedef enum {
     GEMM_TILE_AUTO = 0,          /* 256x256 on a CTA pair if M > 128 and N > 128
                                     (128x128 if the pair tiles would number at
                                     most a quarter of the SMs, 128x256 if at
-                                    most half and K <= 4096), else 128x128
+                                    most half and K <= 4096, 256x512 if
+                                    K >= 8192 and the 256x512 tiles fill at
+                                    least one round of pairs), else 128x128
                                     (N <= 128) or 128x256; gemm_resolve_tile
                                     tells which */
     GEMM_TILE_128x128 = 128,     /* one CTA, K = 128 per stage, stages 1..3 (64 KB each) */
     GEMM_TILE_128x256 = 256,     /* one CTA, K = 64 per stage, stages 1..4 (48 KB each) */
-    GEMM_TILE_256x256_2SM = 512  /* a CTA pair, K = 128 per stage, stages 1..3
+    GEMM_TILE_256x256_2SM = 512, /* a CTA pair, K = 128 per stage, stages 1..3
                                     (64 KB each per CTA) */
+    GEMM_TILE_256x512_2SM = 1024 /* a CTA pair, K = 64 per stage, stages 1..4
+                                    (48 KB each per CTA): two N = 256 MMAs share
+                                    each A stage (a quarter fewer operand bytes
+                                    per FLOP), one 512-column accumulator
+                                    released in halves; bit-identical to the
+                                    256x256 pair tile */
 } gemm_tile_t;
 
 /* Register-fragment scheme of the SIMT sgemm (gemm_ex's `tile` when dtype
@@ -240,8 +250,11 @@ int gemm_schedule_set(int schedule);
  * Arguments, layout, alignment and return codes: as gemm_ex, tensor-core
  * dtypes only (GEMM_F32 gives GEMM_ERR_UNSUPPORTED).  A launch whose
  * workspace (one 128 x tile-width fp32 partial per CTA, plus flags; 19.9 MB
- * for the default tile on 152 SMs) exceeds 20 MiB is refused with
- * GEMM_ERR_SCRATCH before anything is enqueued.
+ * for the 256-wide tiles on 152 SMs) exceeds 20 MiB is refused with
+ * GEMM_ERR_SCRATCH before anything is enqueued: GEMM_TILE_256x512_2SM asked
+ * for by name is.  Where GEMM_TILE_AUTO would pick that tile, this entry point
+ * runs GEMM_TILE_256x256_2SM instead (the same bits; `stages` above 3 is taken
+ * as 3).
  *
  * Every call shares the one array (per GPU).  Each call clears the flags it
  * uses with cudaMemsetAsync on `stream` before its kernel (the array keeps

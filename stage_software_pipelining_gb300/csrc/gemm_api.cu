@@ -35,7 +35,8 @@ int out_size(int dtype) { return dtype == GEMM_BF16_BF16 ? 2 : 4; }
 //     (the same work per SM in the same single round) runs 4-9 % faster
 //     (2048^2 x 1024 / 2048 / 4096); at K = 8192 the pair stays ahead.
 int resolve_tile(int64_t M, int64_t N, int64_t K, int tile) {
-    if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM)
+    if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM ||
+        tile == GEMM_TILE_256x512_2SM)
         return tile;
     if (tile != GEMM_TILE_AUTO) return 0;
     if (M > 128 && N > 128) {
@@ -43,6 +44,12 @@ int resolve_tile(int64_t M, int64_t N, int64_t K, int tile) {
         const int sms = ssp::tc_current_device_sms();
         if (pair_tiles * 4 <= sms) return GEMM_TILE_128x128;
         if (pair_tiles * 2 <= sms && K <= 4096) return GEMM_TILE_128x256;
+        // The 512-wide tile carries a quarter fewer operand bytes per FLOP,
+        // but its epilogue only half overlaps the next tile: it pays once the
+        // mainloop is long (K >= 8192, measured +3-4 %; K = 4096 is even or
+        // worse) and there is at least a full round of wide tiles.
+        const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
+        if (K >= 8192 && wide_tiles * 2 >= sms) return GEMM_TILE_256x512_2SM;
         return GEMM_TILE_256x256_2SM;
     }
     return N <= 128 ? GEMM_TILE_128x128 : GEMM_TILE_128x256;
@@ -53,6 +60,7 @@ int tile_max_stages(int tile) {
         case GEMM_TILE_128x128: return ssp::kTcMaxStages128;
         case GEMM_TILE_128x256: return ssp::kTcMaxStages256;
         case GEMM_TILE_256x256_2SM: return ssp::kTcMaxStagesPair;
+        case GEMM_TILE_256x512_2SM: return ssp::kTcMaxStagesWide;
         default: return 0;
     }
 }
@@ -127,8 +135,8 @@ ssp::TcLaunch tc_request(int64_t M, int64_t N, int64_t K, const void* A, int64_t
     L.out_bf16 = dtype == GEMM_BF16_BF16;
     L.b_col_major = b_col_major;
     L.stages = stages;
-    L.tile_n = tile == GEMM_TILE_128x128 ? 128 : 256;
-    L.pair = tile == GEMM_TILE_256x256_2SM;
+    L.tile_n = tile == GEMM_TILE_128x128 ? 128 : tile == GEMM_TILE_256x512_2SM ? 512 : 256;
+    L.pair = tile == GEMM_TILE_256x256_2SM || tile == GEMM_TILE_256x512_2SM;
     L.wait_limit_ns = g_wait_limit_ns;
     L.withhold_arrive = g_withhold_arrive;
     L.clock_log = g_clock_log;
@@ -324,9 +332,19 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
             cudaStreamWaitEvent(s, hp->in_done[pi], 0) != cudaSuccess)
             return fail();
         // Every panel uses the tile chosen for the whole of M, so that the
-        // panels compute exactly what one call over all of M would.
+        // panels compute exactly what one call over all of M would.  The one
+        // exception gives the same bits: a panel too short to fill a round of
+        // 256 x 512 tiles runs the 256 x 256 pair tile, whose MMAs take every
+        // K step of every output in the same order (at most its 3 stages;
+        // the stage count changes timing only).
+        int ptile = is_tc(dtype) ? v.tile : tile, pstages = stages;
+        if (ptile == GEMM_TILE_256x512_2SM &&
+            resolve_tile(r1 - r0, N, K, GEMM_TILE_AUTO) != GEMM_TILE_256x512_2SM) {
+            ptile = GEMM_TILE_256x256_2SM;
+            pstages = std::min(stages, ssp::kTcMaxStagesPair);
+        }
         st = run(r1 - r0, N, K, need_ab ? pA : hA, lda, need_ab ? dB : B, ldb, pC, ldc, alpha,
-                 beta, dtype, stages, b_col_major, is_tc(dtype) ? v.tile : tile, s);
+                 beta, dtype, pstages, b_col_major, ptile, s);
         if (st != GEMM_OK) {
             fail();
             return st;
@@ -443,8 +461,17 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     if (M == 0 || N == 0) return GEMM_OK;
     if (K == 0 || alpha == 0.0f)
         return ssp::scale_launch(M, N, C, ldc, dtype == GEMM_BF16_BF16, beta, s);
+    // The automatic choice stays within the fixed array: a 256 x 512 tile's
+    // partials (128 x 512 fp32 per CTA) would not fit, and the 256 x 256 pair
+    // tile gives the same bits (at most its 3 stages; the stage count changes
+    // timing only).
+    int t = v.tile;
+    if (tile == GEMM_TILE_AUTO && t == GEMM_TILE_256x512_2SM) {
+        t = GEMM_TILE_256x256_2SM;
+        stages = std::min(stages, ssp::kTcMaxStagesPair);
+    }
     ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages,
-                                 b_col_major, v.tile);
+                                 b_col_major, t);
     L.schedule = 2;  // stream-K tail, its partials in the fixed array
     return ssp::tc_launch_noalloc(L, s);
 }

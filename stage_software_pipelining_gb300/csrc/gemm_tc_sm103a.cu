@@ -250,6 +250,58 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* p, unsigned int v) 
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Epilogue of whole output boxes [ci0, ci1) of one tile for this warp's 32
+// TMEM lanes: each box of 32 rows x 128 bytes (CW = 32 fp32 or 64 bf16
+// columns) is read from TMEM, scaled by alpha, written 128-byte swizzled into
+// the warp's ring of nb boxes and sent by one tensor store, or for REDUCE by
+// one tensor reduce-add into C.  The box width, the output type and the kind
+// of write-back are compile-time, so the loop has no per-box branches: the
+// general loop below, with its runtime tests for edges, stream-K partials and
+// C read-back, issues about twice the instructions per box.
+template <int CW, bool REDUCE>
+__device__ __forceinline__ void epilogue_boxes(const CUtensorMap* tmC, uint32_t t_row,
+                                               uint32_t epi_buf0, int nb, int ci0, int ci1,
+                                               int col0, int row_base, float alpha, int lane) {
+    for (int ci = ci0; ci < ci1; ++ci) {
+        const uint32_t buf = epi_buf0 + static_cast<uint32_t>(ci % nb) * 4096u;
+        // The store that last used this box has read it.
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint32_t r[CW];
+        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(ci * CW),
+                           *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        if constexpr (CW == 64)
+            tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(ci * CW + 32),
+                               *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            uint4 u;
+            if constexpr (CW == 32) {
+                u = make_uint4(__float_as_uint(alpha * __uint_as_float(r[4 * jj])),
+                               __float_as_uint(alpha * __uint_as_float(r[4 * jj + 1])),
+                               __float_as_uint(alpha * __uint_as_float(r[4 * jj + 2])),
+                               __float_as_uint(alpha * __uint_as_float(r[4 * jj + 3])));
+            } else {
+                __nv_bfloat162 h[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    h[e] = __floats2bfloat162_rn(alpha * __uint_as_float(r[8 * jj + 2 * e]),
+                                                 alpha * __uint_as_float(r[8 * jj + 2 * e + 1]));
+                u = *reinterpret_cast<const uint4*>(h);
+            }
+            st_shared_v4(buf + lane * 128 + ((jj ^ (lane & 7)) << 4), u);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            if constexpr (REDUCE) tma_reduce_add_2d(tmC, buf, col0 + ci * CW, row_base);
+            else tma_store_2d(tmC, buf, col0 + ci * CW, row_base);
+            bulk_commit_group();
+        }
+    }
+}
+
 // Named barrier over the four epilogue warps (128 threads).
 __device__ __forceinline__ void epilogue_bar_sync() {
     asm volatile("barrier.sync 1, 128;" ::: "memory");
@@ -270,7 +322,20 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 // between two ring waits).  Each stage costs the MMA thread one wait and one
 // commit, which on GB300 take about as long as a few MMAs: with 4 MMAs per
 // stage the tensor pipe idled ~15 % of the time, with 8 it stays busy.
-template <bool PAIR, int KA>
+//
+// WIDE (a pair, KA = 1): the 256 x 512 tile.  Each K = 16 step is two
+// N = 256 MMAs that share the A operand, so a stage carries a quarter fewer
+// operand bytes per FLOP than two 256 x 256 tiles would.  CTA rank r stages
+// two 128-column pieces of B, tile columns 128r.. and 256 + 128r.., so that
+// MMA h writes tile columns 256h..256h+255 into TMEM columns 256h.. of one
+// 512-column accumulator.  With no second accumulator the epilogue cannot
+// overlap the next tile's whole mainloop, so the accumulator is released in
+// halves: the epilogue frees columns 0..255 first, the next tile's h = 0 MMAs
+// start at once, and each stage's h = 1 MMAs (with the stage's release) wait
+// until columns 256..511 are free too, at most S stages behind.  Both halves
+// still see their K steps in order, so C is bit-identical to the 256-wide
+// pair tile's.
+template <bool PAIR, int KA, bool WIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -278,6 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Swizzled TMA destinations and UMMA operands want 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    static_assert(!WIDE || (PAIR && KA == 1), "the 256 x 512 tile is a CTA pair with K = 64 stages");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
     constexpr int BKS = KA * BK;                       // K per stage
     constexpr int A_STAGE_BYTES = KA * A_ATOM_BYTES;
@@ -306,7 +372,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
     volatile int* abort_flag = &ctl->abort;
-    const uint32_t tmem_cols = 2u * p.bn;  // two accumulators: 256 or 512 columns
+    // Two accumulators of bn columns (256 or 512 in all), or one of 512 (WIDE).
+    const uint32_t tmem_cols = WIDE ? 512u : 2u * p.bn;
     constexpr uint16_t kPairMask = 0x3;
 
     if (threadIdx.x == 0) {
@@ -376,6 +443,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tile_coords(p, job.tile, tm, tn);
                 const int a_row = tm * TILE_M + static_cast<int>(rank) * BM;
                 const int b_col = tn * p.bn + static_cast<int>(rank) * b_cols;
+                // B pieces of this CTA: one of b_cols columns, or (WIDE) two of
+                // 128 columns, tile columns 128r and 256 + 128r.
+                constexpr int NPIECES = WIDE ? 2 : 1;
+                const int pw = b_cols / NPIECES;
                 for (int kt = job.kb; kt < job.ke; ++kt) {
                     if (!bounded_wait<PAIR>(empty_bar(s), ph ^ 1u, abort_flag, p.wait_limit_ns,
                                             ROLE_PRODUCER, it, peer_rank)) {
@@ -395,34 +466,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             for (int a = 0; a < KA; ++a)
                                 tma_load_2d_pair_hint(a_dst + a * A_ATOM_BYTES, &tmA, bar, k0 + a * BK,
                                                       a_row, a_policy);
-                            if (p.b_chunked) {
-                                tma_load_3d_pair(b_dst, &tmB, bar, 0, k0, b_col / 64);
-                            } else if (p.b_mn_major) {
-                                for (int j = 0; j < b_cols / 64; ++j)
-                                    tma_load_2d_pair(b_dst + j * B_CHUNK_BYTES, &tmB, bar,
-                                                     b_col + 64 * j, k0);
-                            } else {
 #pragma unroll
-                                for (int a = 0; a < KA; ++a)
-                                    tma_load_2d_pair(b_dst + a * b_atom_bytes, &tmB, bar, k0 + a * BK,
-                                                     b_col);
+                            for (int pc = 0; pc < NPIECES; ++pc) {
+                                const int bc = WIDE ? tn * p.bn + pc * 256 + static_cast<int>(rank) * pw : b_col;
+                                const uint32_t bd = b_dst + static_cast<uint32_t>(
+                                    pc * (p.b_mn_major ? (pw / 64) * B_CHUNK_BYTES : pw * 128));
+                                if (p.b_chunked) {
+                                    tma_load_3d_pair(bd, &tmB, bar, 0, k0, bc / 64);
+                                } else if (p.b_mn_major) {
+                                    for (int j = 0; j < pw / 64; ++j)
+                                        tma_load_2d_pair(bd + j * B_CHUNK_BYTES, &tmB, bar, bc + 64 * j,
+                                                         k0);
+                                } else {
+#pragma unroll
+                                    for (int a = 0; a < KA; ++a)
+                                        tma_load_2d_pair(bd + a * b_atom_bytes, &tmB, bar, k0 + a * BK,
+                                                         bc);
+                                }
                             }
                         } else {
 #pragma unroll
                             for (int a = 0; a < KA; ++a)
                                 tma_load_2d_hint(a_dst + a * A_ATOM_BYTES, &tmA, full_bar(s),
                                                  k0 + a * BK, a_row, a_policy);
-                            if (p.b_chunked) {
-                                tma_load_3d(b_dst, &tmB, full_bar(s), 0, k0, b_col / 64);
-                            } else if (p.b_mn_major) {
-                                for (int j = 0; j < b_cols / 64; ++j)
-                                    tma_load_2d(b_dst + j * B_CHUNK_BYTES, &tmB, full_bar(s),
-                                                b_col + 64 * j, k0);
-                            } else {
 #pragma unroll
-                                for (int a = 0; a < KA; ++a)
-                                    tma_load_2d(b_dst + a * b_atom_bytes, &tmB, full_bar(s),
-                                                k0 + a * BK, b_col);
+                            for (int pc = 0; pc < NPIECES; ++pc) {
+                                const int bc = WIDE ? tn * p.bn + pc * 256 + static_cast<int>(rank) * pw : b_col;
+                                const uint32_t bd = b_dst + static_cast<uint32_t>(
+                                    pc * (p.b_mn_major ? (pw / 64) * B_CHUNK_BYTES : pw * 128));
+                                if (p.b_chunked) {
+                                    tma_load_3d(bd, &tmB, full_bar(s), 0, k0, bc / 64);
+                                } else if (p.b_mn_major) {
+                                    for (int j = 0; j < pw / 64; ++j)
+                                        tma_load_2d(bd + j * B_CHUNK_BYTES, &tmB, full_bar(s),
+                                                    bc + 64 * j, k0);
+                                } else {
+#pragma unroll
+                                    for (int a = 0; a < KA; ++a)
+                                        tma_load_2d(bd + a * b_atom_bytes, &tmB, full_bar(s),
+                                                    k0 + a * BK, bc);
+                                }
                             }
                         }
                     }
@@ -485,6 +568,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int lt = 0;
             bool ok = true;
             Job job;
+            if constexpr (WIDE) {
+                // One accumulator in two halves: tmem_empty[h] is released by the
+                // epilogue once it has read columns 256h..256h+255.
+                int dq_s[kTcMaxStages], dq_kt[kTcMaxStages];  // stages whose h = 1 MMAs wait
+                for (int j = 0; ok && next_job(p, unit, num_units, j, job); ++j, ++lt) {
+                    const uint32_t tph = static_cast<uint32_t>(lt & 1) ^ 1u;
+                    if (!bounded_wait<PAIR>(tempty_bar(0), tph, abort_flag, p.wait_limit_ns, ROLE_MMA,
+                                            it, peer_rank)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    bool d1 = mbar_try_wait(tempty_bar(1), tph);
+                    if (d1) tc_fence_after();
+                    int nd = 0;
+                    // The stage's MMAs into half h: N = 256, B from piece h (16 KB on).
+                    auto issue_half = [&](int h, int ss, int kt_) {
+                        const uint32_t a_s = a_lo + static_cast<uint32_t>(ss * A_STAGE_BYTES) / 16u;
+                        const uint32_t b_s = b_lo + static_cast<uint32_t>(ss * b_stage_bytes) / 16u +
+                                             static_cast<uint32_t>(h) * (16384u / 16u);
+#pragma unroll
+                        for (int kk = 0; kk < BKS / UMMA_K; ++kk) {
+                            const uint64_t ad = (static_cast<uint64_t>(a_hi) << 32) |
+                                                (a_s + static_cast<uint32_t>(kk) * 2u);
+                            const uint64_t bd = (static_cast<uint64_t>(b_hi) << 32) |
+                                                (b_s + static_cast<uint32_t>(kk) * b_k16);
+                            const uint32_t accum = (kt_ != job.kb || kk != 0) ? 1u : 0u;
+                            umma_f16_pair(tmem_base + static_cast<uint32_t>(h) * 256u, ad, bd, p.idesc,
+                                          accum);
+                        }
+                    };
+                    // Catch up the waiting stages' h = 1 MMAs, in K order, and free their slots.
+                    auto flush = [&]() {
+                        for (int i = 0; i < nd; ++i) {
+                            issue_half(1, dq_s[i], dq_kt[i]);
+                            umma_commit_pair_multicast(empty_bar(dq_s[i]), kPairMask);
+                        }
+                        nd = 0;
+                    };
+                    for (int kt = job.kb; kt < job.ke; ++kt) {
+                        if (!bounded_wait<PAIR>(full_bar(s), ph, abort_flag, p.wait_limit_ns,
+                                                ROLE_MMA, it, peer_rank)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_half(0, s, kt);
+                        if (!d1) {
+                            d1 = mbar_try_wait(tempty_bar(1), tph);
+                            if (d1) tc_fence_after();
+                        }
+                        if (d1) {
+                            flush();
+                            issue_half(1, s, kt);
+                            umma_commit_pair_multicast(empty_bar(s), kPairMask);
+                        } else {
+                            dq_s[nd] = s;
+                            dq_kt[nd] = kt;
+                            if (++nd == S) {  // every slot is held: wait for the second half
+                                if (!bounded_wait<PAIR>(tempty_bar(1), tph, abort_flag,
+                                                        p.wait_limit_ns, ROLE_MMA, it, peer_rank)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                d1 = true;
+                                flush();
+                            }
+                        }
+                        ++it;
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (!d1) {
+                        if (!bounded_wait<PAIR>(tempty_bar(1), tph, abort_flag, p.wait_limit_ns,
+                                                ROLE_MMA, it, peer_rank)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    flush();
+                    // accumulator ready for the epilogue (of both CTAs)
+                    umma_commit_pair_multicast(tfull_bar(0), kPairMask);
+                }
+            } else {
             for (int j = 0; ok && next_job(p, unit, num_units, j, job); ++j, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
@@ -529,6 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if constexpr (PAIR) umma_commit_pair_multicast(tfull_bar(acc), kPairMask);
                 else umma_commit(tfull_bar(acc));
             }
+            }
             if (!ok) {
                 // Wait for every MMA this thread issued before TMEM is freed.
                 if constexpr (PAIR) umma_commit_pair_multicast(drain_bar, 0x1);
@@ -564,8 +737,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int lt = 0;
         Job job;
         for (int j = 0; next_job(p, unit, num_units, j, job); ++j, ++lt) {
-            const int acc = lt & 1;
-            const uint32_t acc_ph = static_cast<uint32_t>((lt >> 1) & 1);
+            const int acc = WIDE ? 0 : (lt & 1);
+            const uint32_t acc_ph = static_cast<uint32_t>(WIDE ? (lt & 1) : ((lt >> 1) & 1));
             int tm, tn;
             tile_coords(p, job.tile, tm, tn);
             const int row_base = tm * TILE_M + static_cast<int>(rank) * BM + 32 * q;  // this warp's rows
@@ -633,7 +806,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // i of chunk ci of warp q's lane l at ((q * nchunks + ci) * cw/4 + i) * 32 + l,
             // so that each warp access is 512 contiguous bytes.
             const size_t my_slot_off = (static_cast<size_t>(unit) * ctas_per_unit + rank) * slot_floats;
-            for (int ci = 0; ci < nchunks; ++ci) {
+            // Whole tile, nothing read back: the branch-free box loop.
+            const bool fast = job.role == JOB_FULL && !job_loads_c && row_base < p.M &&
+                              col0 + p.bn <= p.N;
+            if (fast) {
+                auto boxes = [&](int c0, int c1) {
+                    if (p.out_bf16)
+                        epilogue_boxes<64, false>(&tmC, t_row, epi_buf0, nb, c0, c1, col0, row_base,
+                                                  p.alpha, lane);
+                    else if (reduce_c)
+                        epilogue_boxes<32, true>(&tmC, t_row, epi_buf0, nb, c0, c1, col0, row_base,
+                                                 p.alpha, lane);
+                    else
+                        epilogue_boxes<32, false>(&tmC, t_row, epi_buf0, nb, c0, c1, col0, row_base,
+                                                  p.alpha, lane);
+                };
+                const int nh = WIDE ? nchunks / 2 : nchunks;
+                boxes(0, nh);
+                if constexpr (WIDE) {
+                    // Columns 0..255 are read: the next tile's first half may start.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader0);
+                }
+                boxes(nh, nchunks);
+            }
+            for (int ci = 0; !fast && ci < nchunks; ++ci) {
                 const int c = ci * cw;
                 const int col_base = col0 + c;
                 const int b = ci % nb;
@@ -797,8 +995,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) {
-                if constexpr (PAIR) mbar_arrive_cluster(tempty_leader0 + 8u * acc);
-                else mbar_arrive(tempty_bar(acc));
+                if constexpr (WIDE) {
+                    if (!fast) mbar_arrive_cluster(tempty_leader0);  // both halves at once
+                    mbar_arrive_cluster(tempty_leader0 + 8u);
+                } else if constexpr (PAIR) {
+                    mbar_arrive_cluster(tempty_leader0 + 8u * acc);
+                } else {
+                    mbar_arrive(tempty_bar(acc));
+                }
             }
         }
         // C copies still in flight after an abort land before the CTA exits.
@@ -905,29 +1109,31 @@ int device_sms(int dev) {
 
 // 64-deep K atoms per stage: 2 (K = 128 per stage, 8 MMAs between ring
 // waits) except for the one-CTA 128 x 256 tile, whose 96 KB stages would
-// leave room for only two; it keeps 48 KB stages of K = 64.
-int stage_atoms(bool pair, int bn) { return (!pair && bn == 256) ? 1 : 2; }
+// leave room for only two, and the 256 x 512 pair tile, whose stages of
+// K = 64 already hold 8 MMAs (two N = 256 MMAs per K = 16 step): both keep
+// 48 KB stages of K = 64.
+int stage_atoms(bool pair, int bn) { return ((!pair && bn == 256) || (pair && bn == 512)) ? 1 : 2; }
 
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
 
-// The kernel instance for a tile and stage depth.
-TcKernel kernel_for(bool pair, int ka) {
-    if (pair) return gemm_tc_kernel<true, 2>;
-    return ka == 1 ? gemm_tc_kernel<false, 1> : gemm_tc_kernel<false, 2>;
+// The kernel instance for a tile and stage depth (wide: the 256 x 512 pair tile).
+TcKernel kernel_for(bool pair, int ka, bool wide) {
+    if (pair) return wide ? gemm_tc_kernel<true, 1, true> : gemm_tc_kernel<true, 2, false>;
+    return ka == 1 ? gemm_tc_kernel<false, 1, false> : gemm_tc_kernel<false, 2, false>;
 }
 
 // The kernels' dynamic shared-memory limit is a per-device attribute.
-bool smem_attribute(int dev, bool pair, int ka) {
+bool smem_attribute(int dev, bool pair, int ka, bool wide) {
     static std::mutex mu;
-    static bool done[64][2][2] = {};
+    static bool done[64][2][2][2] = {};
     std::lock_guard<std::mutex> g(mu);
     if (dev < 0 || dev >= 64 || ka < 1 || ka > 2) return false;
-    if (!done[dev][pair][ka - 1]) {
+    if (!done[dev][pair][ka - 1][wide]) {
         const cudaError_t e = cudaFuncSetAttribute(
-            kernel_for(pair, ka), cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
-        done[dev][pair][ka - 1] = e == cudaSuccess;
+            kernel_for(pair, ka, wide), cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
+        done[dev][pair][ka - 1][wide] = e == cudaSuccess;
     }
-    return done[dev][pair][ka - 1];
+    return done[dev][pair][ka - 1][wide];
 }
 
 // Launch configuration: clusters of `cluster` CTAs (2 for the pair tile),
@@ -959,23 +1165,25 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid,
 
 // Number of CTA pairs that can be resident at once for a given shared-memory
 // size (cached per device and size).
-int max_resident_pairs(int dev, size_t smem) {
+int max_resident_pairs(int dev, size_t smem, bool wide) {
     static std::mutex mu;
-    static size_t key_smem[64][8] = {};
-    static int val[64][8] = {};
+    static size_t key_smem[64][2][8] = {};
+    static int val[64][2][8] = {};
     std::lock_guard<std::mutex> g(mu);
     if (dev < 0 || dev >= 64) return 0;
     for (int i = 0; i < 8; ++i)
-        if (key_smem[dev][i] == smem && val[dev][i] > 0) return val[dev][i];
+        if (key_smem[dev][wide][i] == smem && val[dev][wide][i] > 0) return val[dev][wide][i];
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     launch_config(&cfg, attr, 2, 2, smem, nullptr, false);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, 2), &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, wide ? 1 : 2, wide), &cfg) !=
+        cudaSuccess)
+        n = 0;
     for (int i = 0; i < 8; ++i)
-        if (key_smem[dev][i] == 0 || i == 7) {
-            key_smem[dev][i] = smem;
-            val[dev][i] = n;
+        if (key_smem[dev][wide][i] == 0 || i == 7) {
+            key_smem[dev][wide][i] = smem;
+            val[dev][wide][i] = n;
             break;
         }
     return n;
@@ -987,6 +1195,7 @@ struct Geometry {
     size_t smem = 0;   // dynamic shared memory per CTA
     int units = 0;     // persistent workers (CTAs, or CTA pairs)
     int ka = 2;        // 64-deep K atoms per stage
+    bool wide = false; // the 256 x 512 pair tile
     size_t ws_bytes = 0;  // stream-K workspace (partials + flags), 0 if unused
 };
 
@@ -1035,7 +1244,9 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.num_tiles = p.tiles_m * p.tiles_n;
     const int ka = stage_atoms(pair, bn);
     const int bks = ka * BK;
+    const bool wide = pair && bn == 512;
     geo.ka = ka;
+    geo.wide = wide;
     p.k_tiles = static_cast<int>((L.K + bks - 1) / bks);
     p.group_m = pair ? 8 : 16;
     p.stages = S;
@@ -1046,10 +1257,10 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     // Instruction descriptor (kind::f16): D fp32 (bit 4), A and B type
     // (bits 7..9, 10..12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B major
     // (bit 16: 1 = MN-major), N >> 3 at bits 17..22, M >> 4 at bits 24..28
-    // (M = 256 across a CTA pair).
+    // (M = 256 across a CTA pair; N = 256 per MMA on the 512-wide tile).
     const uint32_t fmt = L.in_bf16 ? 1u : 0u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(p.b_mn_major) << 16) |
-              (static_cast<uint32_t>(bn >> 3) << 17) |
+              (static_cast<uint32_t>((bn > 256 ? 256 : bn) >> 3) << 17) |
               (static_cast<uint32_t>(tile_m >> 4) << 24);
     p.alpha = L.alpha;
     p.beta = L.beta;
@@ -1067,7 +1278,7 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
     const int sms = device_sms(dev);
     if (sms <= 0) return GEMM_ERR_CUDA;
-    if (!smem_attribute(dev, pair, ka)) return GEMM_ERR_LAUNCH;
+    if (!smem_attribute(dev, pair, ka, wide)) return GEMM_ERR_LAUNCH;
 
     // The operand ring, then as many output boxes per epilogue warp (up to
     // kEpiMaxBufs) as the 227 KB of shared memory leave room for.
@@ -1086,7 +1297,7 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     geo.smem = smem;
     int max_units = sms;
     if (pair) {
-        max_units = max_resident_pairs(dev, smem);
+        max_units = max_resident_pairs(dev, smem, wide);
         if (max_units <= 0) return GEMM_ERR_LAUNCH;
     }
     // Stream-K tail: when the last round of full tiles would leave units idle,
@@ -1122,7 +1333,9 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
 // of them per stage.
 bool encode_maps(const TcLaunch& L, int bks, bool chunked, CUtensorMap* tmA, CUtensorMap* tmB,
                  CUtensorMap* tmC, int* b_chunked) {
-    const int b_cols = L.pair ? L.tile_n / 2 : L.tile_n;
+    // Columns per B box: the CTA's half of the tile, or a 128-column piece of
+    // it on the 512-wide tile.
+    const int b_cols = L.pair ? (L.tile_n >= 512 ? 128 : L.tile_n / 2) : L.tile_n;
     if (!encode_c(tmC, L.C, L.out_bf16, L.M, L.N, L.ldc)) return false;
     if (!encode_2d(tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return false;
     *b_chunked = (chunked && !L.b_col_major && L.N % 64 == 0) ? 1 : 0;
@@ -1136,7 +1349,7 @@ int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     launch_config(&cfg, attr, geo.grid, geo.cluster, geo.smem, stream, true);
-    if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.ka), tmA, tmB, tmC, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.ka, geo.wide), tmA, tmB, tmC, p) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }

@@ -28,8 +28,8 @@ struct TcLaunch {
     int out_bf16;     // 0 fp32 output, 1 bf16 output
     int b_col_major;  // 0 B row-major (N contiguous), 1 B column-major (K contiguous)
     int stages;       // ring depth (1..3, or 1..4 for the 128 x 256 tile)
-    int tile_n;       // tile width: 128 or 256
-    int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256
+    int tile_n;       // tile width: 128, 256 or (pair only) 512
+    int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256 or 512
     int schedule;     // 0 auto, 1 full tiles only, 2 stream-K tail whenever a round is partial
     int64_t wait_limit_ns;
     int withhold_arrive;
@@ -90,7 +90,8 @@ constexpr int kCopyMaxStages = 8;
 constexpr int kTcMaxStages128 = 3;   // 128 x 128 x 128 tile: 64 KB per stage
 constexpr int kTcMaxStages256 = 4;   // 128 x 256 x 64 tile: 48 KB per stage
 constexpr int kTcMaxStagesPair = 3;  // 256 x 256 x 128 tile on a CTA pair: 64 KB per stage per CTA
-constexpr int kTcMaxStages = 4;      // the largest of the three
+constexpr int kTcMaxStagesWide = 4;  // 256 x 512 x 64 tile on a CTA pair: 48 KB per stage per CTA
+constexpr int kTcMaxStages = 4;      // the largest of the four
 constexpr int kSimtMaxStages = 4;
 
 }  // namespace ssp

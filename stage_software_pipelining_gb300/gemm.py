@@ -31,6 +31,10 @@ TILE_AUTO = 0
 TILE_128x128 = 128
 TILE_128x256 = 256
 TILE_256x256_2SM = 512
+TILE_256x512_2SM = 1024
+
+# Deepest ring each tensor-core tile has shared memory for (gemm_max_stages).
+TILE_MAX_STAGES = {TILE_128x128: 3, TILE_128x256: 4, TILE_256x256_2SM: 3, TILE_256x512_2SM: 4}
 
 # SIMT register-fragment schemes (gemm_simt_fragments_t), passed as `tile` for fp32
 SIMT_FRAGMENTS_DOUBLE = 0
@@ -153,11 +157,21 @@ def _args(A, B, C):
     return M, N, K, lda, ldb, bcm, ldc, dtype_code(A.dtype, C.dtype)
 
 
-def default_stages(dtype: int) -> int:
-    """Ring depth used when a call passes none: 2 on the SIMT path; 3 on the
-    tensor-core path (the deepest ring of the 128 x 128 and pair tiles, and a
-    valid depth for every tile)."""
-    return 2 if dtype == GEMM_F32 else 3
+def default_stages(dtype: int, tile: int | None = None) -> int:
+    """Ring depth used when a call passes none: 2 on the SIMT path; on the
+    tensor-core path the deepest ring the (resolved) tile has room for, which
+    is also its fastest (3 when no tile is given: valid for every tile)."""
+    if dtype == GEMM_F32:
+        return 2
+    return TILE_MAX_STAGES.get(tile, 3)
+
+
+def _stages_for(stages, code: int, M: int, N: int, K: int, tile: int) -> int:
+    if stages is not None:
+        return int(stages)
+    if code == GEMM_F32:
+        return default_stages(code)
+    return default_stages(code, resolve_tile(M, N, K, code, tile))
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
@@ -174,8 +188,12 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
     if not (A.is_cuda and B.is_cuda and C.is_cuda):
         raise ValueError("A, B and C must be CUDA tensors (use gemm_host for host buffers)")
     M, N, K, lda, ldb, bcm, ldc, code = _args(A, B, C)
-    st = default_stages(code) if stages is None else int(stages)
     dev = C.device.index
+    if stages is None and dev != torch.cuda.current_device():
+        with torch.cuda.device(dev):
+            st = _stages_for(stages, code, M, N, K, tile)
+    else:
+        st = _stages_for(stages, code, M, N, K, tile)
     s = (stream or torch.cuda.current_stream(dev)).cuda_stream
     lib = _lib or load_library()
     fn = lib.gemm_checked if checked else lib.gemm_ex
@@ -200,7 +218,7 @@ def gemm_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 
         if t.device.type != "cpu":
             raise ValueError(f"{n} must be a host tensor")
     M, N, K, lda, ldb, bcm, ldc, code = _args(A, B, C)
-    st = default_stages(code) if stages is None else int(stages)
+    st = _stages_for(stages, code, M, N, K, tile)
     s = (stream or torch.cuda.current_stream()).cuda_stream
     status = load_library().gemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
                                       C.data_ptr(), ldc, float(alpha), float(beta), code, st,

@@ -70,12 +70,14 @@ def test_bad_dtype_and_stages(lib):
     assert gemm_ex(lib, 8, 8, 8, stages=7) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=5) == G.GEMM_ERR_ARG
     # shared memory holds at most 3 stages of K = 128 for the 128 x 128 and
-    # pair tiles and 4 of K = 64 for the 128 x 256 tile; no tile takes 5
+    # 256 x 256 pair tiles and 4 of K = 64 for the 128 x 256 and 256 x 512
+    # tiles; no tile takes 5
     assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_256x256_2SM) == G.GEMM_ERR_UNSUPPORTED
     assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_128x128) == G.GEMM_ERR_UNSUPPORTED
     assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_128x256) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_256x512_2SM) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, tile=192) == G.GEMM_ERR_ARG
-    assert gemm_ex(lib, 8, 8, 8, tile=1024) == G.GEMM_ERR_ARG
+    assert gemm_ex(lib, 8, 8, 8, tile=2048) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=128) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=2) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, bcm=2) == G.GEMM_ERR_ARG
@@ -136,8 +138,11 @@ def test_resolve_tile_without_a_device(lib):
     """Explicit tiles come back unchanged; SIMT types and bad codes are
     refused; on a host without a GPU the automatic choice is the pair tile
     for large M and N and the one-CTA tiles for a single 128-row/column."""
-    for t in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM):
+    for t in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM):
         assert lib.gemm_resolve_tile(4096, 4096, 4096, GEMM_BF16_F32, t) == t
+    # long K takes the 512-wide pair tile, shorter K the 256-wide one
+    assert lib.gemm_resolve_tile(4096, 4096, 8192, GEMM_BF16_F32, 0) == G.TILE_256x512_2SM
+    assert lib.gemm_resolve_tile(4096, 4096, 4096, GEMM_BF16_F32, 0) == G.TILE_256x256_2SM
     assert lib.gemm_resolve_tile(8, 8, 8, GEMM_F32, 0) == G.GEMM_ERR_ARG
     assert lib.gemm_resolve_tile(8, 8, 8, GEMM_BF16_F32, 192) == G.GEMM_ERR_ARG
     assert lib.gemm_resolve_tile(-1, 8, 8, GEMM_BF16_F32, 0) == G.GEMM_ERR_ARG
@@ -151,6 +156,7 @@ def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 3
     assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 3
+    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_256x512_2SM) == 4
     assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 4
     assert lib.gemm_max_stages(GEMM_F32, 128) == G.GEMM_ERR_ARG
     assert lib.gemm_max_stages(9, 0) == G.GEMM_ERR_ARG

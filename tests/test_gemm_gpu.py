@@ -115,9 +115,9 @@ def test_simt_register_fragment_schemes_agree_bitwise(stages):
 
 
 # --------------------------------------------------------------------------- tensor cores
-TILES = [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM]
+TILES = [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM]
 TILE_STAGES = {G.TILE_128x128: [1, 2, 3], G.TILE_128x256: [1, 2, 3, 4],
-               G.TILE_256x256_2SM: [1, 2, 3]}
+               G.TILE_256x256_2SM: [1, 2, 3], G.TILE_256x512_2SM: [1, 2, 3, 4]}
 
 
 @pytest.mark.parametrize("dtype", TC_DTYPES)
@@ -248,12 +248,15 @@ def G_in(dtype):
 
 def test_automatic_tile_choice_on_gb300():
     """The automatic tile on this GPU: the pair tile once the pair tiles fill
-    more than half the SMs (or K is long), 128 x 256 for one partial round at
-    K <= 4096, 128 x 128 when the pair tiles would busy at most a quarter."""
+    more than half the SMs (or K is long), its 512-wide form when K >= 8192
+    and the wide tiles fill a round of pairs, 128 x 256 for one partial round
+    at K <= 4096, 128 x 128 when the pair tiles would busy at most a quarter."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert sms >= 128
     dt = GEMM_BF16_F32
-    assert G.resolve_tile(8192, 8192, 8192, dt) == G.TILE_256x256_2SM
+    assert G.resolve_tile(8192, 8192, 8192, dt) == G.TILE_256x512_2SM
+    assert G.resolve_tile(4096, 4096, 8192, dt) == G.TILE_256x512_2SM   # 128 wide tiles
+    assert G.resolve_tile(8192, 8192, 4096, dt) == G.TILE_256x256_2SM
     assert G.resolve_tile(2048, 2048, 2048, dt) == G.TILE_128x256     # 64 pair tiles
     assert G.resolve_tile(2048, 2048, 8192, dt) == G.TILE_256x256_2SM
     assert G.resolve_tile(1024, 1024, 4096, dt) == G.TILE_128x128     # 16 pair tiles
@@ -267,7 +270,7 @@ def test_empty_m_or_n_is_a_noop():
 
 
 # --------------------------------------------------------------------------- fault path
-@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM])
+@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM])
 def test_withheld_arrive_times_out_and_context_survives(tile):
     """Block 0's producer skips one stage: the MMA wait must run out, the
     kernel must return GEMM_ERR_TIMEOUT (no hang, no trap), and the next
@@ -326,6 +329,26 @@ def test_host_entry_in_row_panels_matches_device_entry(dtype, beta):
                          what=f"gemm_host panels dt={dtype} beta={beta}")
 
 
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_host_panels_of_a_wide_tile_call_give_its_bits(beta):
+    """A long-K call resolves to the 256 x 512 tile, but its 256-row panels
+    are too short for a round of those tiles and run the 256 x 256 pair tile
+    (at its own stage limit): the bits must still be the device call's."""
+    M, N, K = 4096, 4096, 8192    # 128 wide tiles: a round of pairs
+    dtype = GEMM_BF16_F32
+    assert G.resolve_tile(M, N, K, dtype) == G.TILE_256x512_2SM
+    assert G.resolve_tile(M // 16, N, K, dtype) != G.TILE_256x512_2SM
+    w = workload(dtype, M, N, K, beta=beta)
+    inp = make_inputs(w)
+    if inp.C0 is None:
+        inp = dataclasses.replace(inp, C0=torch.zeros(M, N, dtype=OUT_DTYPE[dtype]))
+    out_dev, _ = run_gpu(inp, 4, tile=G.TILE_256x512_2SM, beta=beta)
+    Ch = inp.C0.clone().pin_memory()
+    G.gemm_host(inp.A.pin_memory(), inp.B.pin_memory(), Ch, w.alpha, beta, stages=4,
+                tile=G.TILE_256x512_2SM)
+    assert np.array_equal(Ch.double().numpy(), out_dev)
+
+
 # --------------------------------------------------------------------------- full-size workloads
 def sample_indices(M, N, count, seed):
     rng = np.random.default_rng(seed)
@@ -342,11 +365,13 @@ def sample_indices(M, N, count, seed):
     ("fp32_2048", 2, 0),
     ("fp16_2048", 3, 0),
     ("bf16_8192_beta1", 4, G.TILE_128x256),
-    ("bf16_8192_beta1", 3, G.TILE_256x256_2SM),     # the configuration bench.py times
+    ("bf16_8192_beta1", 4, G.TILE_256x512_2SM),     # the configuration bench.py times
+    ("bf16_8192_beta1", 3, G.TILE_256x256_2SM),
     ("bf16_8192_beta1", 3, G.TILE_128x128),
     ("bf16_ragged_colB", 4, G.TILE_128x256),
     ("bf16_ragged_colB", 3, G.TILE_256x256_2SM),
     ("bf16_ragged_colB", 2, G.TILE_256x256_2SM),
+    ("bf16_ragged_colB", 4, G.TILE_256x512_2SM),
 ])
 def test_full_size_workload_sampled(name, stages, tile):
     w = BY_NAME[name]
@@ -387,6 +412,24 @@ def test_full_size_stage_sweep_is_bitwise_invariant():
                 base = C
             else:
                 assert torch.equal(C, base), f"tile={tile} stages={s}"
+
+
+@pytest.mark.parametrize("dtype", TC_DTYPES)
+@pytest.mark.parametrize("b_col_major", [False, True])
+@pytest.mark.parametrize("beta", [0.0, 1.0, -0.75])
+def test_wide_tile_is_bitwise_the_pair_tile(dtype, b_col_major, beta):
+    """The 256 x 512 tile issues each output's K = 16 steps in the same order
+    as the 256 x 256 pair tile (two N = 256 MMAs per step instead of one), so
+    C must come out bit for bit the same, on a ragged shape that leaves
+    partial wide tiles in both M and N, with C read back (beta != 0, 1),
+    added at L2 (beta = 1, fp32 C) or not read (beta = 0)."""
+    w = workload(dtype, 700, 1100, 900, alpha=1.25, beta=beta, b_col_major=b_col_major)
+    inp = make_inputs(w)
+    pair, _ = run_gpu(inp, 3, tile=G.TILE_256x256_2SM)
+    wide, _ = run_gpu(inp, 4, tile=G.TILE_256x512_2SM)
+    assert np.array_equal(pair, wide)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(wide, ref, absb, dtype, beta=beta, C0=inp.C0, what="wide tile")
 
 
 @pytest.mark.parametrize("M,N,K", [(1_048_581, 136, 40),    # 4097 pair-tile rows, ragged
@@ -477,8 +520,8 @@ def test_stream_k_workspace_reused_across_tiles(stream_k):
     wherever an earlier call left its partials."""
     inp = make_inputs(workload(GEMM_BF16_F32, 768, 1280, 1024, beta=0.0))
     ref, absb = oracle_full(inp)
-    for tile in (G.TILE_256x256_2SM, G.TILE_128x128, G.TILE_128x256, G.TILE_128x128,
-                 G.TILE_256x256_2SM):
+    for tile in (G.TILE_256x512_2SM, G.TILE_256x256_2SM, G.TILE_128x128, G.TILE_128x256,
+                 G.TILE_128x128, G.TILE_256x512_2SM):
         out, _ = run_gpu(inp, 2, tile=tile)
         check_against_oracle(out, ref, absb, GEMM_BF16_F32, what=f"stream-K reuse tile={tile}")
 
@@ -496,7 +539,7 @@ def test_stream_k_schedules_agree_within_tolerance():
         G.schedule_set(G.SCHEDULE_AUTO)
 
 
-@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM])
+@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM])
 def test_stream_k_timeout_leaves_context_usable(stream_k, tile):
     inp = make_inputs(workload(GEMM_BF16_F32, 512, 768, 1024, beta=0.0))
     A = to_device_padded(inp.A)

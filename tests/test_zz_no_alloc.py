@@ -105,3 +105,27 @@ def test_noalloc_matches_oracle_at_the_headline_shape(lib):
     c0s = inp.C0[torch.from_numpy(rows), torch.from_numpy(cols)]
     check_against_oracle(got, ref, absb, GEMM_BF16_F32, beta=w.beta, C0=c0s,
                          what="gemm_noalloc 8192^3")
+
+
+def test_noalloc_automatic_tile_stays_within_the_array(lib):
+    """A long-K call whose automatic tile would be the 256 x 512 one (its
+    partials do not fit the fixed array) runs the 256 x 256 pair tile and
+    agrees with gemm_ex; naming the 256 x 512 tile is refused up front."""
+    M, N, K = 2304, 4608, 8192
+    assert G.resolve_tile(M, N, K, GEMM_BF16_F32) == G.TILE_256x512_2SM
+    w = BY_NAME["bf16_8192_beta1"].resized(M, N, K)
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    C_ex = inp.C0.cuda()
+    C = inp.C0.cuda()
+    assert call(lib.gemm_ex, A, B, C_ex, w.alpha, w.beta, w.dtype, 4, 0) == G.GEMM_OK
+    st = call(lib.gemm_noalloc, A, B, C, w.alpha, w.beta, w.dtype, 4, 0)
+    assert st == G.GEMM_OK, G.status_string(st)
+    torch.cuda.synchronize()
+    _, absb = oracle.gemm(inp.A[:64], inp.B, inp.C0[:64], w.alpha, w.beta)
+    got = C[:64].double().cpu().numpy()
+    ex = C_ex[:64].double().cpu().numpy()
+    assert np.all(np.abs(got - ex) <= 2e-3 * absb)
+    C2 = inp.C0.cuda()
+    assert call(lib.gemm_noalloc, A, B, C2, w.alpha, w.beta, w.dtype, 4,
+                G.TILE_256x512_2SM) == G.GEMM_ERR_SCRATCH
