@@ -19,7 +19,8 @@
 //   * the release is tcgen05.commit, which arrives on the stage's "empty"
 //     barrier once the MMAs reading it have finished;
 //   * the CTA is persistent and keeps two accumulators in TMEM, so the
-//     epilogue of one output tile overlaps the mainloop of the next;
+//     epilogue of one output tile overlaps the mainloop of the next (the
+//     256 x 512 tile has room for one, and releases it in halves);
 //   * a stage holds K = 128 (8 MMAs) so that the per-stage wait and commit
 //     stay off the tensor pipe's critical path;
 //   * the epilogue moves C with tensor copies (and, for beta = 1 with fp32 C,
