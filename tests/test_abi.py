@@ -247,3 +247,13 @@ def test_cublas_comparison_entry_parses_without_a_gpu():
                        cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert "--launches" in r.stdout
+
+
+def test_default_stages_follow_the_tile():
+    # the deepest ring each tile has room for; 3 (valid everywhere) without one
+    assert G.default_stages(GEMM_F32) == 2
+    assert G.default_stages(GEMM_BF16_F32) == 3
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_128x128) == 3
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_256x256_2SM) == 3
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_256x512_2SM) == 4
