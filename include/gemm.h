@@ -132,7 +132,9 @@ typedef enum {
  *              beta != 0 and written
  *   dtype      a gemm_dtype_t
  *   stages     depth of the shared-memory ring: 1..3 on the tensor-core path
- *              (1..4 for the 128 x 256 tile), 1..4 on the SIMT path
+ *              (1..4 for the 128 x 256 and 256 x 512 tiles), 1..4 on the SIMT
+ *              path; gemm_max_stages gives a tile's limit and a deeper ring
+ *              than the resolved tile holds is GEMM_ERR_UNSUPPORTED
  *   stream     cudaStream_t
  * The tensor-core tile is GEMM_TILE_AUTO's choice.
  */
