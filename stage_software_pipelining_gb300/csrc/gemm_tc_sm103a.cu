@@ -21,8 +21,9 @@
 //   * the CTA is persistent and keeps two accumulators in TMEM, so the
 //     epilogue of one output tile overlaps the mainloop of the next (the
 //     256 x 512 tile has room for one, and releases it in halves);
-//   * a stage holds K = 128 (8 MMAs) so that the per-stage wait and commit
-//     stay off the tensor pipe's critical path;
+//   * a stage holds 8 MMAs (K = 128; K = 64 with two N = 256 MMAs per K step
+//     on the 256 x 512 tile) so that the per-stage wait and commit stay off
+//     the tensor pipe's critical path;
 //   * the epilogue moves C with tensor copies (and, for beta = 1 with fp32 C,
 //     adds into C at L2 with tensor reduces), and consecutive GEMMs on a
 //     stream overlap their prologue through programmatic dependent launch.
