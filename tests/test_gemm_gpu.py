@@ -432,6 +432,23 @@ def test_wide_tile_is_bitwise_the_pair_tile(dtype, b_col_major, beta):
     check_against_oracle(wide, ref, absb, dtype, beta=beta, C0=inp.C0, what="wide tile")
 
 
+@pytest.mark.parametrize("tile", [G.TILE_256x256_2SM, G.TILE_256x512_2SM])
+def test_back_to_back_launches_are_deterministic(tile):
+    """200 launches in a row on one stream (consecutive grids overlap through
+    programmatic dependent launch; the 256 x 512 tile also hands its
+    accumulator over in halves) leave exactly the bits of one checked call."""
+    w = workload(GEMM_BF16_BF16, 2048, 4096, 8192, beta=0.0, b_col_major=False)
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    one = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    G.gemm(A, B, one, 1.0, 0.0, stages=G.TILE_MAX_STAGES[tile], tile=tile, checked=True)
+    many = torch.empty_like(one)
+    for _ in range(200):
+        G.gemm(A, B, many, 1.0, 0.0, stages=G.TILE_MAX_STAGES[tile], tile=tile)
+    G.gemm(A, B, many, 1.0, 0.0, stages=G.TILE_MAX_STAGES[tile], tile=tile, checked=True)
+    assert torch.equal(one, many)
+
+
 @pytest.mark.parametrize("M,N,K", [(1_048_581, 136, 40),    # 4097 pair-tile rows, ragged
                                    (130, 200, 131_080)])    # 1025 stages of K = 128
 def test_extreme_dimensions_sampled(M, N, K):
