@@ -355,11 +355,16 @@ def run_ours(args):
                 "kernel": "gemm_tc_kernel", "mean_launch_ms": round(launch_ms, 4)}
         # The per-SM tensor rate measured on this GPU (after the timed region):
         # the GEMM against SMs x that rate x the clock sampled under load.
-        rate = G.mma_rate(n_mma=8192)
+        # The per-SM tensor rate of the instruction this tile issues: the
+        # CTA-pair form for the 256-row tiles, the one-CTA form otherwise.
+        pair_tile = tile in (G.TILE_256x256_2SM, G.TILE_256x512_2SM)
+        rate = G.mma_rate(n_mma=8192, pair=pair_tile)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         per_clock = {"flop_per_clk_per_sm": round(rate["flop_per_clk_per_sm"], 1),
-                     "probe": f"{rate['ctas']} CTAs x {rate['n_mma']} tcgen05.mma 128x256x16, "
-                              f"SM clocks per CTA {rate['cycles_min']}..{rate['cycles_max']}",
+                     "probe": (f"{rate['ctas'] // 2} CTA pairs x {rate['n_mma']} tcgen05.mma."
+                               f"cta_group::2 256x256x16" if pair_tile else
+                               f"{rate['ctas']} CTAs x {rate['n_mma']} tcgen05.mma 128x256x16")
+                              + f", SM clocks {rate['cycles_min']}..{rate['cycles_max']}",
                      "peak_at_max_clock": round(rate["flop_per_clk_per_sm"] * sms
                                                 * peaks.get("sm_max_mhz", 2070.0) * 1e-6, 1)}
         if kernel_mhz:

@@ -311,6 +311,21 @@ int pipelined_copy(void* dst, const void* src, int64_t n_bytes, int stages, void
 int mma_rate(int n_mma, int ctas, long long* cycles, float* elapsed_ms);
 
 /*
+ * mma_rate_pair -- mma_rate for the CTA-pair instruction the 256-row tiles
+ * issue: `pairs` clusters of two CTAs (on two SMs each) allocate TMEM across
+ * the pair, and each leader issues n_mma tcgen05.mma.cta_group::2 (M = 256,
+ * N = 256, K = 16; each CTA supplies 128 rows of A and 128 columns of B),
+ * timing them on its SM clock.  Per SM this is again 2*128*256*16 FLOP per
+ * instruction.
+ *   n_mma        1 .. 2^20 MMAs per pair (GEMM_ERR_ARG otherwise)
+ *   pairs        1 .. half the device's SM count (GEMM_ERR_ARG otherwise)
+ *   cycles       host array of `pairs` entries, written: each leader's SM clocks
+ *   elapsed_ms   host pointer, written: CUDA-event time of the launch
+ * Synchronous, on the legacy default stream; GEMM_ERR_TIMEOUT as mma_rate.
+ */
+int mma_rate_pair(int n_mma, int pairs, long long* cycles, float* elapsed_ms);
+
+/*
  * gemm_debug_set -- test hook for the bounded waits (not thread-safe; affects
  * later launches of the tensor-core kernel from this process).
  *   wait_limit_ns      time a pipeline wait may spin before it gives up

@@ -45,7 +45,7 @@ EXPORTS = ("gemm", "gemm_ex", "gemm_checked", "gemm_host", "gemm_host_release",
            "gemm_status_string", "gemm_max_stages", "gemm_plan", "gemm_debug_set",
            "gemm_resolve_tile",
            "pipelined_copy", "gemm_schedule_set", "gemm_noalloc", "mma_rate",
-           "gemm_clock_log")
+           "gemm_clock_log", "mma_rate_pair")
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_schedule_set.restype = i32
         lib.mma_rate.argtypes = [i32, i32, p, p]
         lib.mma_rate.restype = i32
+        lib.mma_rate_pair.argtypes = [i32, i32, p, p]
+        lib.mma_rate_pair.restype = i32
         lib.gemm_clock_log.argtypes = [p]
         lib.gemm_clock_log.restype = i32
         if path == LIB_PATH:
@@ -279,22 +281,28 @@ def pipelined_copy(dst: torch.Tensor, src: torch.Tensor, stages: int = 2,
 MMA_RATE_FLOPS = 2 * 128 * 256 * 16
 
 
-def mma_rate(n_mma: int = 8192, ctas: int | None = None, device: int | None = None) -> dict:
+def mma_rate(n_mma: int = 8192, ctas: int | None = None, device: int | None = None,
+             pair: bool = False) -> dict:
     """Dense bf16 tensor-pipe rate in FLOP per SM per clock (libgemm.so
     mma_rate): `ctas` CTAs (default: one per SM) each issue n_mma
-    back-to-back 128 x 256 x 16 MMAs and count SM clocks.  Synchronous."""
+    back-to-back 128 x 256 x 16 MMAs and count SM clocks.  With pair=True
+    (mma_rate_pair) ctas/2 CTA pairs each issue n_mma 256 x 256 x 16
+    cta_group::2 MMAs, the same FLOP per SM per instruction.  Synchronous."""
     dev = torch.cuda.current_device() if device is None else int(device)
     if ctas is None:
         ctas = torch.cuda.get_device_properties(dev).multi_processor_count
-    cycles = (ctypes.c_longlong * int(ctas))()
+    units = int(ctas) // 2 if pair else int(ctas)
+    cycles = (ctypes.c_longlong * units)()
     ms = ctypes.c_float()
+    fn = load_library().mma_rate_pair if pair else load_library().mma_rate
     with torch.cuda.device(dev):
-        st = load_library().mma_rate(int(n_mma), int(ctas), cycles, ctypes.byref(ms))
+        st = fn(int(n_mma), units, cycles, ctypes.byref(ms))
     if st != GEMM_OK:
-        raise GemmError(st, "mma_rate")
+        raise GemmError(st, "mma_rate_pair" if pair else "mma_rate")
     cyc = sorted(int(c) for c in cycles)
     flops = n_mma * MMA_RATE_FLOPS
-    return {"n_mma": int(n_mma), "ctas": int(ctas),
+    ctas = 2 * units if pair else units
+    return {"n_mma": int(n_mma), "ctas": int(ctas), "pair": bool(pair),
             "cycles_min": cyc[0], "cycles_median": cyc[len(cyc) // 2], "cycles_max": cyc[-1],
             "flop_per_clk_per_sm": flops / cyc[len(cyc) // 2],
             "elapsed_ms": ms.value,

@@ -257,3 +257,13 @@ def test_default_stages_follow_the_tile():
     assert G.default_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
     assert G.default_stages(GEMM_BF16_F32, G.TILE_256x256_2SM) == 3
     assert G.default_stages(GEMM_BF16_F32, G.TILE_256x512_2SM) == 4
+
+
+def test_mma_rate_pair_argument_checks(lib):
+    cyc = (ctypes.c_longlong * 4)()
+    ms = ctypes.c_float()
+    assert lib.mma_rate_pair(0, 2, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate_pair((1 << 20) + 1, 2, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate_pair(16, 0, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate_pair(16, 2, None, ctypes.byref(ms)) == G.GEMM_ERR_ARG
+    assert lib.mma_rate_pair(16, 2, cyc, None) == G.GEMM_ERR_ARG

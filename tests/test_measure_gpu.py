@@ -31,6 +31,20 @@ def test_rate_on_every_sm():
     assert r["cycles_max"] <= 1.05 * r["cycles_min"], r
 
 
+def test_pair_rate_on_every_tpc():
+    """The CTA-pair instruction of the 256-row tiles runs at the same rate
+    per SM as the one-CTA one."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    r = G.mma_rate(n_mma=8192, pair=True)
+    assert r["ctas"] == sms - sms % 2 and r["pair"]
+    assert r["cycles_min"] > 0
+    rate = r["flop_per_clk_per_sm"]
+    assert 0.9 * NOMINAL_FLOP_PER_CLK <= rate <= 1.01 * NOMINAL_FLOP_PER_CLK, r
+    assert r["cycles_max"] <= 1.05 * r["cycles_min"], r
+    one = G.mma_rate(n_mma=64, ctas=2, pair=True)
+    assert one["cycles_min"] > 0
+
+
 @pytest.mark.parametrize("n_mma", [1, 3, 4096])
 def test_small_counts_and_one_cta(n_mma):
     r = G.mma_rate(n_mma=n_mma, ctas=1)
