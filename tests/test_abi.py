@@ -267,3 +267,31 @@ def test_mma_rate_pair_argument_checks(lib):
     assert lib.mma_rate_pair(16, 0, cyc, ctypes.byref(ms)) == G.GEMM_ERR_ARG
     assert lib.mma_rate_pair(16, 2, None, ctypes.byref(ms)) == G.GEMM_ERR_ARG
     assert lib.mma_rate_pair(16, 2, cyc, None) == G.GEMM_ERR_ARG
+
+
+def test_binding_constants_match_the_header():
+    """Every enum value include/gemm.h declares is the value the Python side
+    passes: status codes, tensor-core tiles, SIMT fragment schemes, dtypes,
+    and each tile's stage limit as gemm_max_stages reports it."""
+    import re
+    from stage_software_pipelining_gb300 import workloads as W
+    text = open(HEADER).read()
+    declared = {name: int(val) for name, val in
+                re.findall(r"\b(GEMM_[A-Z0-9_x]+)\s*=\s*(-?\d+)", text)}
+    expect = {
+        "GEMM_OK": G.GEMM_OK, "GEMM_ERR_ARG": G.GEMM_ERR_ARG,
+        "GEMM_ERR_UNSUPPORTED": G.GEMM_ERR_UNSUPPORTED, "GEMM_ERR_ALIGN": G.GEMM_ERR_ALIGN,
+        "GEMM_ERR_LAUNCH": G.GEMM_ERR_LAUNCH, "GEMM_ERR_TIMEOUT": G.GEMM_ERR_TIMEOUT,
+        "GEMM_ERR_CUDA": G.GEMM_ERR_CUDA, "GEMM_ERR_SCRATCH": G.GEMM_ERR_SCRATCH,
+        "GEMM_TILE_AUTO": G.TILE_AUTO, "GEMM_TILE_128x128": G.TILE_128x128,
+        "GEMM_TILE_128x256": G.TILE_128x256, "GEMM_TILE_256x256_2SM": G.TILE_256x256_2SM,
+        "GEMM_TILE_256x512_2SM": G.TILE_256x512_2SM,
+        "GEMM_SIMT_FRAGMENTS_DOUBLE": G.SIMT_FRAGMENTS_DOUBLE,
+        "GEMM_SIMT_FRAGMENTS_SINGLE": G.SIMT_FRAGMENTS_SINGLE,
+        "GEMM_F32": W.GEMM_F32, "GEMM_F16_F32": W.GEMM_F16_F32,
+        "GEMM_BF16_F32": W.GEMM_BF16_F32, "GEMM_BF16_BF16": W.GEMM_BF16_BF16,
+    }
+    assert declared == expect
+    lib = G.load_library()
+    for tile, stages in G.TILE_MAX_STAGES.items():
+        assert lib.gemm_max_stages(W.GEMM_BF16_F32, tile) == stages
