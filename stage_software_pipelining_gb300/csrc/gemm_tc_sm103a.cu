@@ -110,7 +110,8 @@ struct Job {
 };
 
 struct SharedCtl {
-    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], drain (on the 256 x 512
+    // tile: tmem_full[0] for the one accumulator, tmem_empty[h] for its halves)
     unsigned long long bar[2 * kTcMaxStages + 5];
     unsigned long long cbar[4 * kEpiMaxBufs];  // C box copies, per epilogue warp and box
     uint32_t tmem_base;
