@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--stages", type=int, default=0, help="0 = the workload's default")
     ap.add_argument("--tile", type=int, default=0,
                     help="tensor-core tile code: 0 auto, 128 (128x128), 256 (128x256), "
-                         "512 (256x256 on a CTA pair)")
+                         "512 (256x256 on a CTA pair), 1024 (256x512 on a CTA pair)")
     ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
                     help="tensor-core tile schedule: 0 the library's automatic choice, "
                          "1 whole tiles, 2 stream-K tail")
@@ -102,13 +102,14 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-TILE_NAMES = {128: "128x128x128 (1 SM)", 256: "128x256x64 (1 SM)",
-              512: "256x256x128 (CTA pair, cta_group::2)",
+TILE_NAMES = {128: "128x128x64 (1 SM)", 256: "128x256x64 (1 SM)",
+              512: "256x256x64 (CTA pair, cta_group::2)",
               1024: "256x512x64 (CTA pair, cta_group::2, two N=256 MMAs per K step)"}
-TILE_MAX_STAGES = {128: 3, 256: 4, 512: 3, 1024: 4}
+# Every stage is a K slice of 64; the deepest ring each tile has room for.
+TILE_MAX_STAGES = {128: 6, 256: 4, 512: 6, 1024: 4}
 SCHEDULE_NAMES = {0: "automatic", 1: "whole tiles", 2: "stream-K tail"}
 # Default ring depth per tile: the deepest ring that fits.
-TILE_DEFAULT_STAGES = {128: 3, 256: 4, 512: 3, 1024: 4}
+TILE_DEFAULT_STAGES = dict(TILE_MAX_STAGES)
 
 
 def committed_traffic(workload: str, stages: int, tile: int):
@@ -218,11 +219,11 @@ def run_ours(args):
 
     w = BY_NAME[args.workload]
     tile = args.tile
-    if w.dtype != GEMM_F32 and tile == 0:
-        tile = G.resolve_tile(w.M, w.N, w.K, w.dtype)   # the library's automatic choice
     if w.dtype == GEMM_F32:
         stages = args.stages or 2
     else:
+        if tile == 0:   # the library's automatic choice (for the ring asked for, if any)
+            tile = G.resolve_tile(w.M, w.N, w.K, w.dtype, stages=args.stages or 4)
         stages = args.stages or TILE_DEFAULT_STAGES[tile]
     inp = make_inputs(w)
     A = inp.A.to(dev)
@@ -338,8 +339,24 @@ def run_ours(args):
         G.load_library().gemm_host_release()
 
     peaks, peak_kind = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = peaks.get("sm_max_mhz", 2070.0)
     if w.dtype == GEMM_F32:
-        roof = None
+        # FP32 FMA pipe: 128 lanes per SM, 2 FLOP per fused multiply-add.
+        achieved = flops_step / (launch_ms * 1e-3) / 1e12
+        peak = sms * 128 * 2 * max_mhz * 1e-6
+        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"FP32 FMA pipe: {sms} SMs x 128 lanes x 2 FLOP x {max_mhz:g} MHz "
+                             f"(max SM clock)",
+                "algorithmic_flops_per_launch": flops_step,
+                "algorithmic_bytes_per_launch": algorithmic_bytes(w),
+                "kernel": "sgemm_simt_kernel", "mean_launch_ms": round(launch_ms, 4)}
+        if clocks and clocks.get("sm_mhz"):
+            pk = sms * 128 * 2 * clocks["sm_mhz"] * 1e-6
+            roof["at_sampled_clock"] = {"sm_mhz": clocks["sm_mhz"], "peak": round(pk, 1),
+                                        "frac": round(achieved / pk, 4)}
+        roof["model"] = roofline_model(w, flops_step, achieved, peak, peaks)
     else:
         sustained = elapsed_ms > 1000.0
         peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
@@ -359,14 +376,15 @@ def run_ours(args):
         # CTA-pair form for the 256-row tiles, the one-CTA form otherwise.
         pair_tile = tile in (G.TILE_256x256_2SM, G.TILE_256x512_2SM)
         rate = G.mma_rate(n_mma=8192, pair=pair_tile)
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         per_clock = {"flop_per_clk_per_sm": round(rate["flop_per_clk_per_sm"], 1),
                      "probe": (f"{rate['ctas'] // 2} CTA pairs x {rate['n_mma']} tcgen05.mma."
                                f"cta_group::2 256x256x16" if pair_tile else
                                f"{rate['ctas']} CTAs x {rate['n_mma']} tcgen05.mma 128x256x16")
                               + f", SM clocks {rate['cycles_min']}..{rate['cycles_max']}",
                      "peak_at_max_clock": round(rate["flop_per_clk_per_sm"] * sms
-                                                * peaks.get("sm_max_mhz", 2070.0) * 1e-6, 1)}
+                                                * max_mhz * 1e-6, 1)}
+        per_clock["frac_at_max_clock"] = round(achieved / per_clock["peak_at_max_clock"], 4)
+        per_clock["frac_of_nominal_dense"] = round(achieved / NOMINAL_DENSE_TFLOPS, 4)
         if kernel_mhz:
             # the clock the GEMM itself ran at (CTA 0's clock64 over globaltimer)
             pk = rate["flop_per_clk_per_sm"] * sms * kernel_mhz * 1e-6
@@ -374,6 +392,8 @@ def run_ours(args):
                               "peak_at_kernel_clock": round(pk, 1),
                               "frac": round(achieved / pk, 4)})
         roof["per_clock"] = per_clock
+        roof["model"] = roofline_model(w, flops_step, achieved, per_clock["peak_at_max_clock"],
+                                       peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -405,6 +425,28 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+NOMINAL_HBM_GBS = 8000.0        # the "8 TB/s-class" HBM3e figure
+NOMINAL_DENSE_TFLOPS = 2250.0   # GB300 dense bf16/fp16 tensor rate, nominal
+
+
+def roofline_model(w, flops, achieved, compute_peak, peaks):
+    """The roofline of the workload: min(compute peak, arithmetic intensity x
+    HBM bandwidth), with the bandwidth both as measured (copy) and nominal."""
+    b = algorithmic_bytes(w)
+    ai = flops / b
+    hbm_meas = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = {"arithmetic_intensity_flop_per_byte": round(ai, 1),
+           "compute_peak_tflops": round(compute_peak, 1)}
+    for key, bw in (("measured", hbm_meas), ("nominal_8tbs", NOMINAL_HBM_GBS)):
+        hbm_bound = ai * bw / 1000.0
+        roof = min(compute_peak, hbm_bound)
+        out[key] = {"hbm_gbs": bw, "hbm_bound_tflops": round(hbm_bound, 1),
+                    "roofline_tflops": round(roof, 1),
+                    "bound": "compute" if compute_peak <= hbm_bound else "hbm",
+                    "frac": round(achieved / roof, 4)}
+    return out
+
+
 def describe(w):
     from stage_software_pipelining_gb300.workloads import IN_DTYPE, OUT_DTYPE
     i = str(IN_DTYPE[w.dtype]).replace("torch.", "")
@@ -427,7 +469,8 @@ def algorithmic_bytes(w) -> int:
 
 # ----------------------------------------------------------------------------- CPU oracle
 def _oracle_block(inp, r0, r1, c0, c1, nthreads=0):
-    """Time the oracle on the block C[r0:r1, c0:c1] of the workload."""
+    """Time the oracle on the block C[r0:r1, c0:c1] of the workload
+    (nthreads 0: every host core)."""
     import oracle
     w = inp.workload
     B = inp.B[:, c0:c1]
@@ -460,10 +503,31 @@ def cpu_baseline(inp, budget_s: float):
         rows = max(rows, min(w.M, rows * int(want_cols / w.N)))
     dt = _oracle_block(inp, 0, rows, 0, cols)
     flops = 2.0 * rows * cols * w.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"C[0:{rows}, 0:{cols}] of the {w.name} workload (K={w.K}) = "
-                      f"{flops:.3e} FLOP, fp64 i-k-j loop, one row per OpenMP thread"}
+    out = {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
+           "threads": cores, "kind": "oracle", "seconds": round(dt, 2),
+           "sample": f"C[0:{rows}, 0:{cols}] of the {w.name} workload (K={w.K}) = "
+                     f"{flops:.3e} FLOP, fp64 i-k-j loop, one row per OpenMP thread"}
+    if w.name in SINGLE_THREAD_WORKLOADS:
+        out["single_thread"] = cpu_single_thread(inp, budget_s=4.0)
+    return out
+
+
+# The three smaller workloads are also timed on one host thread.
+SINGLE_THREAD_WORKLOADS = ("fp32_256", "fp32_2048", "fp16_2048")
+
+
+def cpu_single_thread(inp, budget_s: float):
+    """The oracle on ONE host thread, on whole rows of C (the whole problem
+    when it fits the budget)."""
+    w = inp.workload
+    t1 = _oracle_block(inp, 0, 1, 0, w.N, nthreads=1)      # one row
+    rows = int(max(1, min(w.M, budget_s / max(t1, 1e-9))))
+    dt = _oracle_block(inp, 0, rows, 0, w.N, nthreads=1)
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "threads": 1,
+            "seconds": round(dt, 3),
+            "sample": f"C[0:{rows}, 0:{w.N}] of the {w.name} workload (K={w.K}) = "
+                      f"{flops:.3e} FLOP" + (" (the whole problem)" if rows == w.M else "")}
 
 
 def run_reference(args):
@@ -568,8 +632,8 @@ def run_copy(args):
             "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic (seeded)",
-            "config": {"workload": "copy_1g: dst = src, 1 GiB, 16-byte cp.async per thread "
-                                   "through an N-stage shared-memory ring, grid-stride",
+            "config": {"workload": "copy_1g: dst = src, 1 GiB, 8 KB bulk copies (TMA) in and "
+                                   "out of an N-slot shared-memory ring per CTA, grid-stride",
                        "stages": stages,
                        "l2": "1 GiB read + 1 GiB written per step > 129 MB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],

@@ -19,9 +19,9 @@
  * a load phase and a compute phase per K tile, stages = 2 is double
  * buffering, stages >= 3 is a multi-stage ring.  The stage count changes
  * timing only: for one dtype and tile, every stage count gives bit-identical C.
- * A tensor-core stage holds a K slice of 128 (of 64 for the 128 x 256 and
- * 256 x 512 tiles) of both operands: 8 tcgen05.mma instructions per ring wait
- * (4 on the 128 x 256 tile).
+ * A tensor-core stage holds a K slice of 64 of both operands on every tile
+ * (one 128-byte swizzle row of 16-bit data): 4 tcgen05.mma instructions per
+ * ring wait (8 on the 256 x 512 tile, two N = 256 MMAs per K step).
  *
  * Layout (all row-major, leading dimensions in elements):
  *   A  M x K, element (i,k) at A[i*lda + k], lda >= K
@@ -31,10 +31,10 @@
  *
  * Types (`dtype`, input -> output; accumulation is always fp32):
  *   GEMM_F32        fp32 A, B, C      CUDA-core SIMT sgemm, stages 1..4
- *   GEMM_F16_F32    fp16 A, B; fp32 C tcgen05 tensor cores, stages 1..3 or 1..4
- *   GEMM_BF16_F32   bf16 A, B; fp32 C tcgen05 tensor cores, stages 1..3 or 1..4
- *   GEMM_BF16_BF16  bf16 A, B, C      tcgen05 tensor cores, stages 1..3 or 1..4
- *                                     (by tile, see gemm_tile_t);
+ *   GEMM_F16_F32    fp16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
+ *   GEMM_BF16_F32   bf16 A, B; fp32 C tcgen05 tensor cores, stages 1..6
+ *   GEMM_BF16_BF16  bf16 A, B, C      tcgen05 tensor cores, stages 1..6
+ *                                     (1..4 on two tiles, see gemm_tile_t);
  *                                     fp32 result rounded to nearest even
  *   alpha and beta are fp32.  alpha is applied to the fp32 sum, then beta*C
  *   is added (one fp32 multiply-add per element).
@@ -90,13 +90,15 @@ typedef enum {
                                     most half and K <= 4096, 256x512 if
                                     K >= 8192 and the 256x512 tiles fill at
                                     least one round of pairs), else 128x128
-                                    (N <= 128) or 128x256; gemm_resolve_tile
-                                    tells which */
-    GEMM_TILE_128x128 = 128,     /* one CTA, K = 128 per stage, stages 1..3 (64 KB each) */
-    GEMM_TILE_128x256 = 256,     /* one CTA, K = 64 per stage, stages 1..4 (48 KB each) */
-    GEMM_TILE_256x256_2SM = 512, /* a CTA pair, K = 128 per stage, stages 1..3
-                                    (64 KB each per CTA) */
-    GEMM_TILE_256x512_2SM = 1024 /* a CTA pair, K = 64 per stage, stages 1..4
+                                    (N <= 128) or 128x256.  With stages 5 or 6
+                                    the 128x256 and 256x512 choices become
+                                    256x256 on a pair (128x128 when M or N is
+                                    a single tile), whose rings hold 6.
+                                    gemm_resolve_tile tells which */
+    GEMM_TILE_128x128 = 128,     /* one CTA, stages 1..6 (32 KB each) */
+    GEMM_TILE_128x256 = 256,     /* one CTA, stages 1..4 (48 KB each) */
+    GEMM_TILE_256x256_2SM = 512, /* a CTA pair, stages 1..6 (32 KB each per CTA) */
+    GEMM_TILE_256x512_2SM = 1024 /* a CTA pair, stages 1..4
                                     (48 KB each per CTA): two N = 256 MMAs share
                                     each A stage (a quarter fewer operand bytes
                                     per FLOP), one 512-column accumulator
@@ -131,12 +133,12 @@ typedef enum {
  *   C, ldc     device pointer and leading dimension of C (M x N), read when
  *              beta != 0 and written
  *   dtype      a gemm_dtype_t
- *   stages     depth of the shared-memory ring: 1..3 on the tensor-core path
- *              (1..4 for the 128 x 256 and 256 x 512 tiles), 1..4 on the SIMT
- *              path; gemm_max_stages gives a tile's limit and a deeper ring
- *              than the resolved tile holds is GEMM_ERR_UNSUPPORTED
+ *   stages     depth of the shared-memory ring, each stage a K slice of 64:
+ *              1..6 on the tensor-core path, 1..4 on the SIMT path (16 of K
+ *              per stage); anything else is GEMM_ERR_ARG
  *   stream     cudaStream_t
- * The tensor-core tile is GEMM_TILE_AUTO's choice.
+ * The tensor-core tile is GEMM_TILE_AUTO's choice for these sizes and this
+ * stage count (every stage count 1..6 has a tile that holds it).
  */
 int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
          void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, void* stream);
@@ -146,9 +148,10 @@ int gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void
  *   b_col_major  0: B row-major (as gemm); 1: B column-major (element (k,j)
  *                at B[j*ldb + k], ldb >= K).  Column-major B is implemented on
  *                the tensor-core path only (GEMM_ERR_UNSUPPORTED for GEMM_F32).
- *   tile         tensor-core path: a gemm_tile_t; a stage count above the
- *                tile's limit gives GEMM_ERR_UNSUPPORTED.  SIMT path (tile
- *                128 x 64): a gemm_simt_fragments_t.
+ *   tile         tensor-core path: a gemm_tile_t; a stage count in 1..6 above
+ *                an explicit tile's limit (5 or 6 on GEMM_TILE_128x256 or
+ *                GEMM_TILE_256x512_2SM) gives GEMM_ERR_UNSUPPORTED.  SIMT path
+ *                (tile 128 x 64): a gemm_simt_fragments_t.
  */
 int gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
             int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
@@ -191,17 +194,18 @@ int gemm_host_release(void);
 /* Human-readable name of a gemm_status_t (static storage). */
 const char* gemm_status_string(int status);
 
-/* Largest `stages` value accepted for a dtype and tile (as in gemm_ex), or
- * GEMM_ERR_ARG for an unknown combination. */
+/* Largest `stages` value accepted for a dtype and tile (as in gemm_ex; 6 for
+ * GEMM_TILE_AUTO), or GEMM_ERR_ARG for an unknown combination. */
 int gemm_max_stages(int dtype, int tile);
 
 /*
- * gemm_resolve_tile -- the gemm_tile_t that gemm_ex uses for these sizes on
- * the current device when passed `tile` (GEMM_TILE_AUTO resolves to a tile
- * code; an explicit tile comes back unchanged).  GEMM_ERR_ARG for a dtype
- * of the SIMT path, a negative size or an unknown tile code.
+ * gemm_resolve_tile -- the gemm_tile_t that gemm_ex uses for these sizes and
+ * this stage count on the current device when passed `tile` (GEMM_TILE_AUTO
+ * resolves to a tile code; an explicit tile comes back unchanged).
+ * GEMM_ERR_ARG for a dtype of the SIMT path, a negative size, stages outside
+ * 1..6 or an unknown tile code.
  */
-int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile);
+int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile, int stages);
 
 /*
  * gemm_plan -- the launch gemm_ex would make for these sizes, without making
@@ -250,13 +254,14 @@ int gemm_schedule_set(int schedule);
  * process exits), and calls no allocating routine at all.
  *
  * Arguments, layout, alignment and return codes: as gemm_ex, tensor-core
- * dtypes only (GEMM_F32 gives GEMM_ERR_UNSUPPORTED).  A launch whose
- * workspace (one 128 x tile-width fp32 partial per CTA, plus flags; 19.9 MB
- * for the 256-wide tiles on 152 SMs) exceeds 20 MiB is refused with
- * GEMM_ERR_SCRATCH before anything is enqueued: GEMM_TILE_256x512_2SM asked
- * for by name is.  Where GEMM_TILE_AUTO would pick that tile, this entry point
- * runs GEMM_TILE_256x256_2SM instead (the same bits; `stages` above 3 is taken
- * as 3).
+ * dtypes only (GEMM_F32 gives GEMM_ERR_UNSUPPORTED).  The workspace is one
+ * 128 x tile-width fp32 partial per CTA, plus flags: 19.9 MB for the 256-wide
+ * tiles on 152 SMs.  GEMM_TILE_256x512_2SM asked for by name is refused with
+ * GEMM_ERR_SCRATCH for every shape (its partials would take 38 MB); any
+ * other launch whose workspace exceeds 20 MiB (a GPU with more SMs) is
+ * refused the same way.  Both checks come before anything is enqueued.
+ * Where GEMM_TILE_AUTO would pick the 256 x 512 tile, this entry point runs
+ * GEMM_TILE_256x256_2SM instead, with the same `stages` and the same bits.
  *
  * Every call shares the one array (per GPU).  Each call clears the flags it
  * uses with cudaMemsetAsync on `stream` before its kernel (the array keeps
@@ -264,7 +269,9 @@ int gemm_schedule_set(int schedule);
  * different streams, or from different threads -- race on the array: order
  * them on one stream.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) and sets the kernel's shared-memory
- * limit; make that first call before any stream capture on that device.
+ * limit; make that first call before any stream capture on that device.  The
+ * address is then kept until the process exits: resetting the device
+ * (cudaDeviceReset) and calling this entry point again is not supported.
  */
 int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                  int64_t ldb, void* C, int64_t ldc, float alpha, float beta, int dtype, int stages,
@@ -272,15 +279,17 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 
 /*
  * pipelined_copy -- dst[0 .. n_bytes) = src[0 .. n_bytes), streamed through a
- * ring of `stages` shared-memory slots per thread (asynchronous 16-byte
- * copies, grid-stride), asynchronous on `stream`.
+ * ring of `stages` shared-memory slots of 8 KB per CTA (one bulk tensor-engine
+ * copy into a slot and one out of it per chunk, full/empty mbarriers as in
+ * the GEMM's ring, chunks walked grid-stride), asynchronous on `stream`.
  *
- * This is the bandwidth-bound counter-example to the GEMM: the grid-stride
- * copy through a `cuda::pipeline` of "learn-kernels.com, Matrix
- * multiplication" (the listing after "Overlap needs stages"), which
- * "Software Pipelining and Double Buffering" ("When it pays") and the CUDA
- * Handbook ("Asynchronous data movement", closing rule) name as the case
- * where extra stages do not pay.  Its stage sweep is measured by bench.py.
+ * This is the bandwidth-bound counter-example to the GEMM: a copy has no
+ * arithmetic to hide a load behind, which "Software Pipelining and Double
+ * Buffering" ("When it pays"), the CUDA Handbook ("Asynchronous data
+ * movement", closing rule) and the copy example after "Overlap needs stages"
+ * on "learn-kernels.com, Matrix multiplication" name as the case where extra
+ * stages do not pay.  Its stage sweep is measured by bench.py.  A ring wait
+ * that runs out (2 s) leaves dst incomplete; nothing is reported.
  *   dst, src   device pointers, 16-byte aligned, ranges must not overlap
  *              (GEMM_ERR_ARG), owned by the caller
  *   n_bytes    >= 0, a multiple of 16 (GEMM_ERR_ALIGN otherwise); 0 is a no-op

@@ -25,36 +25,6 @@ bool is_tc(int dtype) {
 int in_size(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
 int out_size(int dtype) { return dtype == GEMM_BF16_BF16 ? 2 : 4; }
 
-// Tensor-core tile for a request (0 = invalid tile code).  The default is the
-// 256 x 256 tile on a CTA pair unless M or N is a single 128-wide tile, or
-// the pair tiles make one partial round (measured on GB300, bf16):
-//   * at most a quarter of the SMs busy: 128 x 128 tiles (four per pair
-//     tile, one SM each) still fit in one round and finish in about half the
-//     time (1024^2 x 4096: 459 vs 316 TFLOP/s);
-//   * at most half of them busy and K <= 4096: the one-CTA 128 x 256 tile
-//     (the same work per SM in the same single round) runs 4-9 % faster
-//     (2048^2 x 1024 / 2048 / 4096); at K = 8192 the pair stays ahead.
-int resolve_tile(int64_t M, int64_t N, int64_t K, int tile) {
-    if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM ||
-        tile == GEMM_TILE_256x512_2SM)
-        return tile;
-    if (tile != GEMM_TILE_AUTO) return 0;
-    if (M > 128 && N > 128) {
-        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        const int sms = ssp::tc_current_device_sms();
-        if (pair_tiles * 4 <= sms) return GEMM_TILE_128x128;
-        if (pair_tiles * 2 <= sms && K <= 4096) return GEMM_TILE_128x256;
-        // The 512-wide tile carries a quarter fewer operand bytes per FLOP,
-        // but its epilogue only half overlaps the next tile: it pays once the
-        // mainloop is long (K >= 8192, measured +3-4 %; K = 4096 is even or
-        // worse) and there is at least a full round of wide tiles.
-        const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
-        if (K >= 8192 && wide_tiles * 2 >= sms) return GEMM_TILE_256x512_2SM;
-        return GEMM_TILE_256x256_2SM;
-    }
-    return N <= 128 ? GEMM_TILE_128x128 : GEMM_TILE_128x256;
-}
-
 int tile_max_stages(int tile) {
     switch (tile) {
         case GEMM_TILE_128x128: return ssp::kTcMaxStages128;
@@ -63,6 +33,46 @@ int tile_max_stages(int tile) {
         case GEMM_TILE_256x512_2SM: return ssp::kTcMaxStagesWide;
         default: return 0;
     }
+}
+
+// Tensor-core tile for a request (0 = invalid tile code).  An explicit tile
+// comes back unchanged.  The automatic choice is the 256 x 256 tile on a CTA
+// pair unless M or N is a single 128-wide tile, or the pair tiles make one
+// partial round (measured on GB300, bf16):
+//   * at most a quarter of the SMs busy: 128 x 128 tiles (four per pair
+//     tile, one SM each) still fit in one round and finish in about half the
+//     time (1024^2 x 4096: 459 vs 316 TFLOP/s);
+//   * at most half of them busy and K <= 4096: the one-CTA 128 x 256 tile
+//     (the same work per SM in the same single round) runs 4-9 % faster
+//     (2048^2 x 1024 / 2048 / 4096); at K = 8192 the pair stays ahead.
+// A ring deeper than the chosen tile holds (5 or 6 stages on the 128 x 256
+// or 256 x 512 tile) takes the tile of the same rows per SM that holds it:
+// the 256 x 256 pair tile (128 x 128 when M or N is a single tile).
+int resolve_tile(int64_t M, int64_t N, int64_t K, int tile, int stages) {
+    if (tile == GEMM_TILE_128x128 || tile == GEMM_TILE_128x256 || tile == GEMM_TILE_256x256_2SM ||
+        tile == GEMM_TILE_256x512_2SM)
+        return tile;
+    if (tile != GEMM_TILE_AUTO) return 0;
+    int t;
+    const bool two_d = M > 128 && N > 128;
+    if (two_d) {
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        const int sms = ssp::tc_current_device_sms();
+        const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
+        if (pair_tiles * 4 <= sms) t = GEMM_TILE_128x128;
+        else if (pair_tiles * 2 <= sms && K <= 4096) t = GEMM_TILE_128x256;
+        // The 512-wide tile carries a quarter fewer operand bytes per FLOP,
+        // but its epilogue only half overlaps the next tile: it pays once the
+        // mainloop is long (K >= 8192, measured +3-4 %; K = 4096 is even or
+        // worse) and there is at least a full round of wide tiles.
+        else if (K >= 8192 && wide_tiles * 2 >= sms) t = GEMM_TILE_256x512_2SM;
+        else t = GEMM_TILE_256x256_2SM;
+    } else {
+        t = N <= 128 ? GEMM_TILE_128x128 : GEMM_TILE_128x256;
+    }
+    if (stages > tile_max_stages(t))
+        t = two_d ? GEMM_TILE_256x256_2SM : GEMM_TILE_128x128;
+    return t;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -89,9 +99,9 @@ Checked validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t& lda, c
     if (M < 0 || N < 0 || K < 0) return {GEMM_ERR_ARG, 0};
     if (b_col_major != 0 && b_col_major != 1) return {GEMM_ERR_ARG, 0};
     if (is_tc(dtype)) {
-        r.tile = resolve_tile(M, N, K, tile);
-        if (r.tile == 0) return {GEMM_ERR_ARG, 0};
         if (stages < 1 || stages > ssp::kTcMaxStages) return {GEMM_ERR_ARG, 0};
+        r.tile = resolve_tile(M, N, K, tile, stages);
+        if (r.tile == 0) return {GEMM_ERR_ARG, 0};
         if (stages > tile_max_stages(r.tile)) return {GEMM_ERR_UNSUPPORTED, 0};
     } else {
         if (tile != GEMM_SIMT_FRAGMENTS_DOUBLE && tile != GEMM_SIMT_FRAGMENTS_SINGLE)
@@ -335,16 +345,14 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
         // panels compute exactly what one call over all of M would.  The one
         // exception gives the same bits: a panel too short to fill a round of
         // 256 x 512 tiles runs the 256 x 256 pair tile, whose MMAs take every
-        // K step of every output in the same order (at most its 3 stages;
-        // the stage count changes timing only).
-        int ptile = is_tc(dtype) ? v.tile : tile, pstages = stages;
+        // K step of every output in the same order (and whose ring holds any
+        // depth the wide tile's does).
+        int ptile = is_tc(dtype) ? v.tile : tile;
         if (ptile == GEMM_TILE_256x512_2SM &&
-            resolve_tile(r1 - r0, N, K, GEMM_TILE_AUTO) != GEMM_TILE_256x512_2SM) {
+            resolve_tile(r1 - r0, N, K, GEMM_TILE_AUTO, stages) != GEMM_TILE_256x512_2SM)
             ptile = GEMM_TILE_256x256_2SM;
-            pstages = std::min(stages, ssp::kTcMaxStagesPair);
-        }
         st = run(r1 - r0, N, K, need_ab ? pA : hA, lda, need_ab ? dB : B, ldb, pC, ldc, alpha,
-                 beta, dtype, pstages, b_col_major, ptile, s);
+                 beta, dtype, stages, b_col_major, ptile, s);
         if (st != GEMM_OK) {
             fail();
             return st;
@@ -404,9 +412,10 @@ int gemm_max_stages(int dtype, int tile) {
     return m > 0 ? m : GEMM_ERR_ARG;
 }
 
-int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile) {
+int gemm_resolve_tile(int64_t M, int64_t N, int64_t K, int dtype, int tile, int stages) {
     if (!is_tc(dtype) || M < 0 || N < 0 || K < 0) return GEMM_ERR_ARG;
-    const int t = resolve_tile(M, N, K, tile);
+    if (stages < 1 || stages > ssp::kTcMaxStages) return GEMM_ERR_ARG;
+    const int t = resolve_tile(M, N, K, tile, stages);
     return t != 0 ? t : GEMM_ERR_ARG;
 }
 
@@ -457,19 +466,18 @@ int gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile);
     if (v.status != GEMM_OK) return v.status;
     if (!is_tc(dtype)) return GEMM_ERR_UNSUPPORTED;  // the SIMT kernel has no scratch variant
+    // One 128 x 512 fp32 partial per CTA of the 256 x 512 tile (256 KB, 38 MB
+    // over 152 SMs) does not fit the fixed array: that tile is refused when
+    // asked for by name, whatever the shape, before anything is enqueued.
+    if (tile == GEMM_TILE_256x512_2SM) return GEMM_ERR_SCRATCH;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0) return GEMM_OK;
     if (K == 0 || alpha == 0.0f)
         return ssp::scale_launch(M, N, C, ldc, dtype == GEMM_BF16_BF16, beta, s);
-    // The automatic choice stays within the fixed array: a 256 x 512 tile's
-    // partials (128 x 512 fp32 per CTA) would not fit, and the 256 x 256 pair
-    // tile gives the same bits (at most its 3 stages; the stage count changes
-    // timing only).
-    int t = v.tile;
-    if (tile == GEMM_TILE_AUTO && t == GEMM_TILE_256x512_2SM) {
-        t = GEMM_TILE_256x256_2SM;
-        stages = std::min(stages, ssp::kTcMaxStagesPair);
-    }
+    // Where the automatic choice is the 256 x 512 tile, the 256 x 256 pair
+    // tile runs instead: it gives the same bits, and its ring holds any depth
+    // the wide tile's does.
+    const int t = v.tile == GEMM_TILE_256x512_2SM ? GEMM_TILE_256x256_2SM : v.tile;
     ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, stages,
                                  b_col_major, t);
     L.schedule = 2;  // stream-K tail, its partials in the fixed array

@@ -21,9 +21,10 @@
 //   * the CTA is persistent and keeps two accumulators in TMEM, so the
 //     epilogue of one output tile overlaps the mainloop of the next (the
 //     256 x 512 tile has room for one, and releases it in halves);
-//   * a stage holds 8 MMAs (K = 128; K = 64 with two N = 256 MMAs per K step
-//     on the 256 x 512 tile) so that the per-stage wait and commit stay off
-//     the tensor pipe's critical path;
+//   * a stage is one 64-deep K slice of both operands (one 128-byte swizzle
+//     row of 16-bit data) on every tile, so the stage count alone sets the
+//     ring's depth: 1..6 stages on the 128 x 128 and 256 x 256 tiles (32 KB
+//     per CTA each), 1..4 on the 128 x 256 and 256 x 512 tiles (48 KB);
 //   * the epilogue moves C with tensor copies (and, for beta = 1 with fp32 C,
 //     adds into C at L2 with tensor reduces), and consecutive GEMMs on a
 //     stream overlap their prologue through programmatic dependent launch.
@@ -34,7 +35,7 @@
 // Ring protocol (slot s = i mod S, n = i div S for the i-th K tile a CTA
 // handles): the producer waits empty[s] for parity (n&1)^1, arms full[s] with
 // the stage's byte count and issues the copies; the MMA thread waits full[s]
-// for parity n&1, issues the stage's MMAs (K = 64 * KA per stage, 16 per MMA)
+// for parity n&1, issues the stage's MMAs (K = 64 per stage, 16 per MMA)
 // and commits to empty[s].  With S = 1 the producer's next copy waits for the
 // MMAs of the same slot: the page's single buffer with a load phase and a
 // compute phase.
@@ -321,12 +322,14 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 // leader.  (Relaying the peer's stage through a thread instead costs one
 // remote round trip per stage and capped the pair at ~60 % of the MMA rate.)
 //
-// KA = 64-deep K atoms per pipeline stage (K = 64 * KA per stage, 4 * KA MMAs
-// between two ring waits).  Each stage costs the MMA thread one wait and one
-// commit, which on GB300 take about as long as a few MMAs: with 4 MMAs per
-// stage the tensor pipe idled ~15 % of the time, with 8 it stays busy.
+// A stage is K = 64 (4 MMAs of K = 16 between two ring waits; 8 on the
+// 256 x 512 tile).  Each stage costs the MMA thread one wait and one commit;
+// with the descriptors advanced by plain adds and the pair's peer copies
+// completing on the leader's barrier directly, those stay off the tensor
+// pipe's critical path (measured: six stages of K = 64 run level with three
+// of K = 128 and give the same bits).
 //
-// WIDE (a pair, KA = 1): the 256 x 512 tile.  Each K = 16 step is two
+// WIDE (a pair): the 256 x 512 tile.  Each K = 16 step is two
 // N = 256 MMAs that share the A operand, so a stage carries a quarter fewer
 // operand bytes per FLOP than two 256 x 256 tiles would.  CTA rank r stages
 // two 128-column pieces of B, tile columns 128r.. and 256 + 128r.., so that
@@ -338,7 +341,7 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 // until columns 256..511 are free too, at most S stages behind.  Both halves
 // still see their K steps in order, so C is bit-identical to the 256-wide
 // pair tile's.
-template <bool PAIR, int KA, bool WIDE>
+template <bool PAIR, bool WIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -346,15 +349,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Swizzled TMA destinations and UMMA operands want 1024-byte alignment.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    static_assert(!WIDE || (PAIR && KA == 1), "the 256 x 512 tile is a CTA pair with K = 64 stages");
+    static_assert(!WIDE || PAIR, "the 256 x 512 tile is a CTA pair");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
-    constexpr int BKS = KA * BK;                       // K per stage
-    constexpr int A_STAGE_BYTES = KA * A_ATOM_BYTES;
-    constexpr int B_CHUNK_BYTES = 64 * BKS * 2;        // MN-major B: one 64-column chunk of a stage
+    constexpr int A_STAGE_BYTES = A_ATOM_BYTES;        // 128 rows x K = 64
+    constexpr int B_CHUNK_BYTES = 64 * BK * 2;         // MN-major B: one 64-column chunk of a stage
     const int S = p.stages;
     const int b_cols = PAIR ? p.bn / 2 : p.bn;   // B columns staged by this CTA
-    const int b_atom_bytes = b_cols * BK * 2;    // K-major B: one 64-deep atom
-    const int b_stage_bytes = KA * b_atom_bytes;
+    const int b_stage_bytes = b_cols * BK * 2;   // this CTA's B columns x K = 64
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * A_STAGE_BYTES;
     uint8_t* epi_ring = b_ring + S * b_stage_bytes;  // 4 warps x epi_bufs output boxes
@@ -460,15 +461,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t a_dst = smem_addr(a_ring + s * A_STAGE_BYTES);
                         const uint32_t b_dst = smem_addr(b_ring + s * b_stage_bytes);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), armed_bytes);
-                        // A: KA atoms of 64 K; B: one copy per 64-column chunk
-                        // (MN-major: 128 K rows each) or per 64-deep atom (K-major).
-                        const int k0 = kt * BKS;
+                        // A: one 64 (K) x 128 (rows) box; B: one copy per piece
+                        // (MN-major: all 64-column chunks at once through the 3-D
+                        // map, or one per chunk; K-major: one 64 x pw box).
+                        const int k0 = kt * BK;
                         if (PAIR && !leader) {
                             const uint32_t bar = leader_full0 + 8u * s;
-#pragma unroll
-                            for (int a = 0; a < KA; ++a)
-                                tma_load_2d_pair_hint(a_dst + a * A_ATOM_BYTES, &tmA, bar, k0 + a * BK,
-                                                      a_row, a_policy);
+                            tma_load_2d_pair_hint(a_dst, &tmA, bar, k0, a_row, a_policy);
 #pragma unroll
                             for (int pc = 0; pc < NPIECES; ++pc) {
                                 const int bc = WIDE ? tn * p.bn + pc * 256 + static_cast<int>(rank) * pw : b_col;
@@ -481,17 +480,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         tma_load_2d_pair(bd + j * B_CHUNK_BYTES, &tmB, bar, bc + 64 * j,
                                                          k0);
                                 } else {
-#pragma unroll
-                                    for (int a = 0; a < KA; ++a)
-                                        tma_load_2d_pair(bd + a * b_atom_bytes, &tmB, bar, k0 + a * BK,
-                                                         bc);
+                                    tma_load_2d_pair(bd, &tmB, bar, k0, bc);
                                 }
                             }
                         } else {
-#pragma unroll
-                            for (int a = 0; a < KA; ++a)
-                                tma_load_2d_hint(a_dst + a * A_ATOM_BYTES, &tmA, full_bar(s),
-                                                 k0 + a * BK, a_row, a_policy);
+                            tma_load_2d_hint(a_dst, &tmA, full_bar(s), k0, a_row, a_policy);
 #pragma unroll
                             for (int pc = 0; pc < NPIECES; ++pc) {
                                 const int bc = WIDE ? tn * p.bn + pc * 256 + static_cast<int>(rank) * pw : b_col;
@@ -504,10 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         tma_load_2d(bd + j * B_CHUNK_BYTES, &tmB, full_bar(s),
                                                     bc + 64 * j, k0);
                                 } else {
-#pragma unroll
-                                    for (int a = 0; a < KA; ++a)
-                                        tma_load_2d(bd + a * b_atom_bytes, &tmB, full_bar(s),
-                                                    k0 + a * BK, bc);
+                                    tma_load_2d(bd, &tmB, full_bar(s), k0, bc);
                                 }
                             }
                         }
@@ -546,9 +536,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // -------------------------------------------------------- MMA issuer
-            // K-major operands: 128-byte rows, 8-row groups 1024 bytes apart; one
-            // K=16 step is 32 bytes along the row, the next 64-deep atom starts
-            // one atom further on.  MN-major B: 64-column chunks B_CHUNK_BYTES
+            // K-major operands: 128-byte rows (the stage's K = 64), 8-row groups
+            // 1024 bytes apart; one K=16 step is 32 bytes along the row.
+            // MN-major B: 64-column chunks B_CHUNK_BYTES
             // apart (leading offset), 8-row K groups 1024 bytes apart; one K=16
             // step is 16 rows = 2048 bytes.
             // The descriptors of stage 0's first MMA; every other MMA of the
@@ -561,10 +551,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t a_hi = static_cast<uint32_t>(a_desc0 >> 32);
             const uint32_t b_lo = static_cast<uint32_t>(b_desc0);
             const uint32_t b_hi = static_cast<uint32_t>(b_desc0 >> 32);
-            // B start-address steps (16-byte units) per K=16 and per atom.
+            // B start-address step (16-byte units) per K = 16.
             const uint32_t b_k16 = p.b_mn_major ? 2048u / 16u : 32u / 16u;
-            const uint32_t b_atom16 =
-                p.b_mn_major ? 4u * b_k16 : static_cast<uint32_t>(b_atom_bytes) / 16u;
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -574,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (WIDE) {
                 // One accumulator in two halves: tmem_empty[h] is released by the
                 // epilogue once it has read columns 256h..256h+255.
-                int dq_s[kTcMaxStages], dq_kt[kTcMaxStages];  // stages whose h = 1 MMAs wait
+                int dq_s[kTcMaxStagesWide], dq_kt[kTcMaxStagesWide];  // stages whose h = 1 MMAs wait
                 for (int j = 0; ok && next_job(p, unit, num_units, j, job); ++j, ++lt) {
                     const uint32_t tph = static_cast<uint32_t>(lt & 1) ^ 1u;
                     if (!bounded_wait<PAIR>(tempty_bar(0), tph, abort_flag, p.wait_limit_ns, ROLE_MMA,
@@ -592,7 +580,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t b_s = b_lo + static_cast<uint32_t>(ss * b_stage_bytes) / 16u +
                                              static_cast<uint32_t>(h) * (16384u / 16u);
 #pragma unroll
-                        for (int kk = 0; kk < BKS / UMMA_K; ++kk) {
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint64_t ad = (static_cast<uint64_t>(a_hi) << 32) |
                                                 (a_s + static_cast<uint32_t>(kk) * 2u);
                             const uint64_t bd = (static_cast<uint64_t>(b_hi) << 32) |
@@ -680,12 +668,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a_s = a_lo + static_cast<uint32_t>(s * A_STAGE_BYTES) / 16u;
                     const uint32_t b_s = b_lo + static_cast<uint32_t>(s * b_stage_bytes) / 16u;
 #pragma unroll
-                    for (int kk = 0; kk < BKS / UMMA_K; ++kk) {
-                        const uint32_t ka = static_cast<uint32_t>(kk / 4), k4 = static_cast<uint32_t>(kk % 4);
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t ad = (static_cast<uint64_t>(a_hi) << 32) |
-                                            (a_s + ka * (A_ATOM_BYTES / 16) + k4 * 2u);
+                                            (a_s + static_cast<uint32_t>(kk) * 2u);
                         const uint64_t bd = (static_cast<uint64_t>(b_hi) << 32) |
-                                            (b_s + ka * b_atom16 + k4 * b_k16);
+                                            (b_s + static_cast<uint32_t>(kk) * b_k16);
                         const uint32_t accum = (kt != job.kb || kk != 0) ? 1u : 0u;
                         if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
                         else umma_f16(d_tmem, ad, bd, p.idesc, accum);
@@ -1110,33 +1097,26 @@ int device_sms(int dev) {
     return cache[dev];
 }
 
-// 64-deep K atoms per stage: 2 (K = 128 per stage, 8 MMAs between ring
-// waits) except for the one-CTA 128 x 256 tile, whose 96 KB stages would
-// leave room for only two, and the 256 x 512 pair tile, whose stages of
-// K = 64 already hold 8 MMAs (two N = 256 MMAs per K = 16 step): both keep
-// 48 KB stages of K = 64.
-int stage_atoms(bool pair, int bn) { return ((!pair && bn == 256) || (pair && bn == 512)) ? 1 : 2; }
-
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
 
-// The kernel instance for a tile and stage depth (wide: the 256 x 512 pair tile).
-TcKernel kernel_for(bool pair, int ka, bool wide) {
-    if (pair) return wide ? gemm_tc_kernel<true, 1, true> : gemm_tc_kernel<true, 2, false>;
-    return ka == 1 ? gemm_tc_kernel<false, 1, false> : gemm_tc_kernel<false, 2, false>;
+// The kernel instance for a tile (wide: the 256 x 512 pair tile).
+TcKernel kernel_for(bool pair, bool wide) {
+    if (pair) return wide ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>;
+    return gemm_tc_kernel<false, false>;
 }
 
 // The kernels' dynamic shared-memory limit is a per-device attribute.
-bool smem_attribute(int dev, bool pair, int ka, bool wide) {
+bool smem_attribute(int dev, bool pair, bool wide) {
     static std::mutex mu;
-    static bool done[64][2][2][2] = {};
+    static bool done[64][2][2] = {};
     std::lock_guard<std::mutex> g(mu);
-    if (dev < 0 || dev >= 64 || ka < 1 || ka > 2) return false;
-    if (!done[dev][pair][ka - 1][wide]) {
+    if (dev < 0 || dev >= 64) return false;
+    if (!done[dev][pair][wide]) {
         const cudaError_t e = cudaFuncSetAttribute(
-            kernel_for(pair, ka, wide), cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
-        done[dev][pair][ka - 1][wide] = e == cudaSuccess;
+            kernel_for(pair, wide), cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
+        done[dev][pair][wide] = e == cudaSuccess;
     }
-    return done[dev][pair][ka - 1][wide];
+    return done[dev][pair][wide];
 }
 
 // Launch configuration: clusters of `cluster` CTAs (2 for the pair tile),
@@ -1180,7 +1160,7 @@ int max_resident_pairs(int dev, size_t smem, bool wide) {
     cudaLaunchAttribute attr[2];
     launch_config(&cfg, attr, 2, 2, smem, nullptr, false);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, wide ? 1 : 2, wide), &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_for(true, wide), &cfg) !=
         cudaSuccess)
         n = 0;
     for (int i = 0; i < 8; ++i)
@@ -1197,7 +1177,6 @@ struct Geometry {
     int cluster = 1;   // CTAs per cluster
     size_t smem = 0;   // dynamic shared memory per CTA
     int units = 0;     // persistent workers (CTAs, or CTA pairs)
-    int ka = 2;        // 64-deep K atoms per stage
     bool wide = false; // the 256 x 512 pair tile
     size_t ws_bytes = 0;  // stream-K workspace (partials + flags), 0 if unused
 };
@@ -1245,12 +1224,9 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     p.tiles_m = static_cast<int>((L.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<int>((L.N + bn - 1) / bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    const int ka = stage_atoms(pair, bn);
-    const int bks = ka * BK;
     const bool wide = pair && bn == 512;
-    geo.ka = ka;
     geo.wide = wide;
-    p.k_tiles = static_cast<int>((L.K + bks - 1) / bks);
+    p.k_tiles = static_cast<int>((L.K + BK - 1) / BK);
     p.group_m = pair ? 8 : 16;
     p.stages = S;
     p.bn = bn;
@@ -1281,11 +1257,11 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
     const int sms = device_sms(dev);
     if (sms <= 0) return GEMM_ERR_CUDA;
-    if (!smem_attribute(dev, pair, ka, wide)) return GEMM_ERR_LAUNCH;
+    if (!smem_attribute(dev, pair, wide)) return GEMM_ERR_LAUNCH;
 
     // The operand ring, then as many output boxes per epilogue warp (up to
     // kEpiMaxBufs) as the 227 KB of shared memory leave room for.
-    const size_t base = 1024 + static_cast<size_t>(S) * (ka * A_ATOM_BYTES + b_cols * bks * 2) +
+    const size_t base = 1024 + static_cast<size_t>(S) * (A_ATOM_BYTES + b_cols * BK * 2) +
                         sizeof(SharedCtl);
     const size_t max_smem = kTcMaxSmem;
     int nb = base < max_smem ? static_cast<int>((max_smem - base) / (4 * EPI_BOX_BYTES)) : 0;
@@ -1332,9 +1308,9 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
 // Tensor maps of one call.  A: M x K row-major, boxes of 64 (K) x 128 (M).
 // B column-major (N x K row-major): boxes of 64 (K) x b_cols (N).  B
 // row-major: one 3-D box of b_cols/64 chunks per stage when N is a multiple
-// of 64 and `chunked` is allowed, else boxes of 64 (N) x bks (K), b_cols/64
+// of 64 and `chunked` is allowed, else boxes of 64 (N) x 64 (K), b_cols/64
 // of them per stage.
-bool encode_maps(const TcLaunch& L, int bks, bool chunked, CUtensorMap* tmA, CUtensorMap* tmB,
+bool encode_maps(const TcLaunch& L, bool chunked, CUtensorMap* tmA, CUtensorMap* tmB,
                  CUtensorMap* tmC, int* b_chunked) {
     // Columns per B box: the CTA's half of the tile, or a 128-column piece of
     // it on the 512-wide tile.
@@ -1343,8 +1319,8 @@ bool encode_maps(const TcLaunch& L, int bks, bool chunked, CUtensorMap* tmA, CUt
     if (!encode_2d(tmA, L.A, L.in_bf16, L.M, L.K, L.lda, BK, BM)) return false;
     *b_chunked = (chunked && !L.b_col_major && L.N % 64 == 0) ? 1 : 0;
     if (L.b_col_major) return encode_2d(tmB, L.B, L.in_bf16, L.N, L.K, L.ldb, BK, b_cols);
-    if (*b_chunked) return encode_b_chunked(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, b_cols / 64, bks);
-    return encode_2d(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, bks);
+    if (*b_chunked) return encode_b_chunked(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, b_cols / 64, BK);
+    return encode_2d(tmB, L.B, L.in_bf16, L.K, L.N, L.ldb, 64, BK);
 }
 
 int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -1352,7 +1328,7 @@ int launch_kernel(const Geometry& geo, bool pair, const CUtensorMap& tmA, const 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     launch_config(&cfg, attr, geo.grid, geo.cluster, geo.smem, stream, true);
-    if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.ka, geo.wide), tmA, tmB, tmC, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel_for(pair, geo.wide), tmA, tmB, tmC, p) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
@@ -1366,7 +1342,7 @@ int tc_launch(const TcLaunch& L, cudaStream_t stream) {
     int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_maps(L, geo.ka * BK, true, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
+    if (!encode_maps(L, true, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
     if (geo.ws_bytes) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -1413,7 +1389,7 @@ int tc_launch_noalloc(const TcLaunch& L, cudaStream_t stream) {
     int st = plan(L, p, geo);
     if (st != GEMM_OK) return st;
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_maps(L, geo.ka * BK, false, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
+    if (!encode_maps(L, false, &tmA, &tmB, &tmC, &p.b_chunked)) return GEMM_ERR_LAUNCH;
     if (geo.ws_bytes) {
         if (geo.ws_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH;
         int dev = 0;

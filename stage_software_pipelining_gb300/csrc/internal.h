@@ -27,7 +27,7 @@ struct TcLaunch {
     int in_bf16;      // 0 fp16 inputs, 1 bf16 inputs
     int out_bf16;     // 0 fp32 output, 1 bf16 output
     int b_col_major;  // 0 B row-major (N contiguous), 1 B column-major (K contiguous)
-    int stages;       // ring depth (1..3, or 1..4 for the 128 x 256 tile)
+    int stages;       // ring depth (1..6, or 1..4 for the 128 x 256 and 256 x 512 tiles)
     int tile_n;       // tile width: 128, 256 or (pair only) 512
     int pair;         // 1: 256-row tile on a CTA pair (cta_group::2), tile_n = 256 or 512
     int schedule;     // 0 auto, 1 full tiles only, 2 stream-K tail whenever a round is partial
@@ -85,13 +85,14 @@ int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float
 int copy_launch(void* dst, const void* src, int64_t n_bytes, int stages, cudaStream_t stream);
 constexpr int kCopyMaxStages = 8;
 
-// Tensor-core ring depth limits.  A stage holds K = 128 of both operands
-// (K = 64 for the 128 x 256 tile).
-constexpr int kTcMaxStages128 = 3;   // 128 x 128 x 128 tile: 64 KB per stage
+// Tensor-core ring depth limits.  A stage holds K = 64 of both operands on
+// every tile; the limit is what fits in 227 KB of shared memory next to the
+// epilogue's output boxes.
+constexpr int kTcMaxStages128 = 6;   // 128 x 128 x 64 tile: 32 KB per stage
 constexpr int kTcMaxStages256 = 4;   // 128 x 256 x 64 tile: 48 KB per stage
-constexpr int kTcMaxStagesPair = 3;  // 256 x 256 x 128 tile on a CTA pair: 64 KB per stage per CTA
+constexpr int kTcMaxStagesPair = 6;  // 256 x 256 x 64 tile on a CTA pair: 32 KB per stage per CTA
 constexpr int kTcMaxStagesWide = 4;  // 256 x 512 x 64 tile on a CTA pair: 48 KB per stage per CTA
-constexpr int kTcMaxStages = 4;      // the largest of the four
+constexpr int kTcMaxStages = 6;      // the largest of the four
 constexpr int kSimtMaxStages = 4;
 
 }  // namespace ssp

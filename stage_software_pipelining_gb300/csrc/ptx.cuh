@@ -97,9 +97,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// 2-D tiled bulk tensor copy shared -> global (completion through the bulk
-// async-group of the issuing thread).  Parts of the box outside the tensor
-// are not written.
 // Programmatic dependent launch: let the next grid on the stream (launched
 // with programmatic stream serialization) start, and wait until the grids
 // this one depends on have completed and their memory is visible.
@@ -121,12 +118,36 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src
         : "memory");
 }
 
+// 2-D tiled bulk tensor copy shared -> global (completion through the bulk
+// async-group of the issuing thread).  Parts of the box outside the tensor
+// are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t c0, int32_t c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
         "r"(c0), "r"(c1), "r"(src)
         : "memory");
+}
+
+// Untiled bulk copy of `bytes` from global to shared memory, completing on an
+// mbarrier (transaction bytes).  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Untiled bulk copy of `bytes` from shared to global memory, completing
+// through the bulk async-group of the issuing thread (same alignment rules).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit_group() {

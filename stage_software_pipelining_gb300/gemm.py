@@ -33,8 +33,10 @@ TILE_128x256 = 256
 TILE_256x256_2SM = 512
 TILE_256x512_2SM = 1024
 
-# Deepest ring each tensor-core tile has shared memory for (gemm_max_stages).
-TILE_MAX_STAGES = {TILE_128x128: 3, TILE_128x256: 4, TILE_256x256_2SM: 3, TILE_256x512_2SM: 4}
+# Deepest ring each tensor-core tile has shared memory for (gemm_max_stages);
+# every stage is a K slice of 64.
+TILE_MAX_STAGES = {TILE_128x128: 6, TILE_128x256: 4, TILE_256x256_2SM: 6, TILE_256x512_2SM: 4}
+TC_MAX_STAGES = 6
 
 # SIMT register-fragment schemes (gemm_simt_fragments_t), passed as `tile` for fp32
 SIMT_FRAGMENTS_DOUBLE = 0
@@ -85,7 +87,7 @@ def load_library(path: str = LIB_PATH):
         lib.gemm_max_stages.argtypes = [i32, i32]
         lib.gemm_debug_set.argtypes = [i64, i32]
         lib.gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p, p, p]
-        lib.gemm_resolve_tile.argtypes = [i64, i64, i64, i32, i32]
+        lib.gemm_resolve_tile.argtypes = [i64, i64, i64, i32, i32, i32]
         lib.gemm_resolve_tile.restype = i32
         lib.pipelined_copy.argtypes = [p, p, i64, i32, p]
         lib.pipelined_copy.restype = i32
@@ -162,10 +164,10 @@ def _args(A, B, C):
 def default_stages(dtype: int, tile: int | None = None) -> int:
     """Ring depth used when a call passes none: 2 on the SIMT path; on the
     tensor-core path the deepest ring the (resolved) tile has room for, which
-    is also its fastest (3 when no tile is given: valid for every tile)."""
+    is also its fastest (4 when no tile is given: valid for every tile)."""
     if dtype == GEMM_F32:
         return 2
-    return TILE_MAX_STAGES.get(tile, 3)
+    return TILE_MAX_STAGES.get(tile, 4)
 
 
 def _stages_for(stages, code: int, M: int, N: int, K: int, tile: int) -> int:
@@ -173,7 +175,8 @@ def _stages_for(stages, code: int, M: int, N: int, K: int, tile: int) -> int:
         return int(stages)
     if code == GEMM_F32:
         return default_stages(code)
-    return default_stages(code, resolve_tile(M, N, K, code, tile))
+    # The tile a 4-stage ring resolves to (every tile holds 4), then its deepest ring.
+    return default_stages(code, resolve_tile(M, N, K, code, tile, stages=4))
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0,
@@ -239,9 +242,11 @@ def max_stages(dtype: int, tile: int = TILE_AUTO) -> int:
     return int(load_library().gemm_max_stages(int(dtype), int(tile)))
 
 
-def resolve_tile(M: int, N: int, K: int, dtype: int, tile: int = TILE_AUTO) -> int:
-    """The TILE_* code gemm uses for these sizes on the current device."""
-    t = int(load_library().gemm_resolve_tile(M, N, K, int(dtype), int(tile)))
+def resolve_tile(M: int, N: int, K: int, dtype: int, tile: int = TILE_AUTO,
+                 stages: int = 4) -> int:
+    """The TILE_* code gemm uses for these sizes and this ring depth on the
+    current device."""
+    t = int(load_library().gemm_resolve_tile(M, N, K, int(dtype), int(tile), int(stages)))
     if t < 0:
         raise GemmError(t, "gemm_resolve_tile")
     return t

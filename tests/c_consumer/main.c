@@ -97,9 +97,13 @@ int main(void) {
         bd[i] = from_bf16(bh[i]);
     }
     memcpy(c, c0, sizeof(float) * M * N);
-    st = gemm_host(M, N, K, ah, K, bh, N, c, N, alpha, beta, GEMM_BF16_F32,
-                   gemm_max_stages(GEMM_BF16_F32, GEMM_TILE_AUTO) > 2 ? 3 : 2, 0, GEMM_TILE_AUTO,
-                   NULL);
+    /* the deepest ring the automatic tile choice offers (6 stages of K = 64) */
+    const int stages = gemm_max_stages(GEMM_BF16_F32, GEMM_TILE_AUTO);
+    const int tile = gemm_resolve_tile(M, N, K, GEMM_BF16_F32, GEMM_TILE_AUTO, stages);
+    printf("bf16: %d stages on tile %d\n", stages, tile);
+    if (stages != 6 || tile <= 0) return 1;
+    st = gemm_host(M, N, K, ah, K, bh, N, c, N, alpha, beta, GEMM_BF16_F32, stages, 0,
+                   GEMM_TILE_AUTO, NULL);
     if (st != GEMM_OK) {
         printf("gemm_host (bf16): %s\n", gemm_status_string(st));
         return 1;

@@ -69,13 +69,17 @@ def test_bad_dtype_and_stages(lib):
     assert gemm_ex(lib, 8, 8, 8, stages=0) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, stages=7) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=5) == G.GEMM_ERR_ARG
-    # shared memory holds at most 3 stages of K = 128 for the 128 x 128 and
-    # 256 x 256 pair tiles and 4 of K = 64 for the 128 x 256 and 256 x 512
-    # tiles; no tile takes 5
-    assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_256x256_2SM) == G.GEMM_ERR_UNSUPPORTED
-    assert gemm_ex(lib, 8, 512, 8, stages=4, tile=G.TILE_128x128) == G.GEMM_ERR_UNSUPPORTED
-    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_128x256) == G.GEMM_ERR_ARG
-    assert gemm_ex(lib, 8, 512, 8, stages=5, tile=G.TILE_256x512_2SM) == G.GEMM_ERR_ARG
+    # every stage is a K slice of 64: shared memory holds 6 stages for the
+    # 128 x 128 and 256 x 256 pair tiles and 4 for the 128 x 256 and 256 x 512
+    # tiles; 1..6 is the valid range, a deeper ring than an explicit tile
+    # holds is a valid request this build does not implement
+    for bad in (0, 7, 8, -1):
+        for t in (0, G.TILE_128x128, G.TILE_256x256_2SM):
+            assert gemm_ex(lib, 8, 512, 8, stages=bad, tile=t) == G.GEMM_ERR_ARG
+    for s in (5, 6):
+        assert gemm_ex(lib, 8, 512, 8, stages=s, tile=G.TILE_128x256) == G.GEMM_ERR_UNSUPPORTED
+        assert gemm_ex(lib, 8, 512, 8, stages=s, tile=G.TILE_256x512_2SM) == \
+            G.GEMM_ERR_UNSUPPORTED
     assert gemm_ex(lib, 8, 8, 8, tile=192) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, tile=2048) == G.GEMM_ERR_ARG
     assert gemm_ex(lib, 8, 8, 8, dtype=GEMM_F32, stages=2, tile=128) == G.GEMM_ERR_ARG
@@ -138,26 +142,35 @@ def test_resolve_tile_without_a_device(lib):
     """Explicit tiles come back unchanged; SIMT types and bad codes are
     refused; on a host without a GPU the automatic choice is the pair tile
     for large M and N and the one-CTA tiles for a single 128-row/column."""
+    rt = lib.gemm_resolve_tile
     for t in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM):
-        assert lib.gemm_resolve_tile(4096, 4096, 4096, GEMM_BF16_F32, t) == t
+        assert rt(4096, 4096, 4096, GEMM_BF16_F32, t, 4) == t
     # long K takes the 512-wide pair tile, shorter K the 256-wide one
-    assert lib.gemm_resolve_tile(4096, 4096, 8192, GEMM_BF16_F32, 0) == G.TILE_256x512_2SM
-    assert lib.gemm_resolve_tile(4096, 4096, 4096, GEMM_BF16_F32, 0) == G.TILE_256x256_2SM
-    assert lib.gemm_resolve_tile(8, 8, 8, GEMM_F32, 0) == G.GEMM_ERR_ARG
-    assert lib.gemm_resolve_tile(8, 8, 8, GEMM_BF16_F32, 192) == G.GEMM_ERR_ARG
-    assert lib.gemm_resolve_tile(-1, 8, 8, GEMM_BF16_F32, 0) == G.GEMM_ERR_ARG
-    assert lib.gemm_resolve_tile(100, 4096, 64, GEMM_BF16_F32, 0) == G.TILE_128x256
-    assert lib.gemm_resolve_tile(4096, 100, 64, GEMM_BF16_F32, 0) == G.TILE_128x128
+    assert rt(4096, 4096, 8192, GEMM_BF16_F32, 0, 4) == G.TILE_256x512_2SM
+    assert rt(4096, 4096, 4096, GEMM_BF16_F32, 0, 4) == G.TILE_256x256_2SM
+    assert rt(8, 8, 8, GEMM_F32, 0, 2) == G.GEMM_ERR_ARG
+    assert rt(8, 8, 8, GEMM_BF16_F32, 192, 2) == G.GEMM_ERR_ARG
+    assert rt(-1, 8, 8, GEMM_BF16_F32, 0, 2) == G.GEMM_ERR_ARG
+    assert rt(100, 4096, 64, GEMM_BF16_F32, 0, 4) == G.TILE_128x256
+    assert rt(4096, 100, 64, GEMM_BF16_F32, 0, 4) == G.TILE_128x128
+    # a ring deeper than the automatic tile holds takes the tile of the same
+    # rows per SM that holds six stages; explicit tiles never change
+    assert rt(4096, 4096, 8192, GEMM_BF16_F32, 0, 5) == G.TILE_256x256_2SM
+    assert rt(4096, 4096, 8192, GEMM_BF16_F32, 0, 6) == G.TILE_256x256_2SM
+    assert rt(100, 4096, 64, GEMM_BF16_F32, 0, 6) == G.TILE_128x128
+    assert rt(4096, 4096, 8192, GEMM_BF16_F32, G.TILE_256x512_2SM, 6) == G.TILE_256x512_2SM
+    for bad in (0, 7):
+        assert rt(4096, 4096, 4096, GEMM_BF16_F32, 0, bad) == G.GEMM_ERR_ARG
 
 
 def test_max_stages(lib):
     assert lib.gemm_max_stages(GEMM_F32, 0) == 4
     assert lib.gemm_max_stages(GEMM_F32, 1) == 4      # single register fragment set
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
-    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 3
-    assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 3
+    assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_128x128) == 6
+    assert lib.gemm_max_stages(GEMM_BF16_BF16, G.TILE_256x256_2SM) == 6
     assert lib.gemm_max_stages(GEMM_BF16_F32, G.TILE_256x512_2SM) == 4
-    assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 4
+    assert lib.gemm_max_stages(GEMM_F16_F32, 0) == 6
     assert lib.gemm_max_stages(GEMM_F32, 128) == G.GEMM_ERR_ARG
     assert lib.gemm_max_stages(9, 0) == G.GEMM_ERR_ARG
 
@@ -226,6 +239,17 @@ def test_noalloc_entry_validates_on_the_host(lib):
     assert na(8, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_F32, 2, 0, 0,
               None) == G.GEMM_ERR_UNSUPPORTED
     assert na(0, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 3, 0, 0, None) == G.GEMM_OK
+    # the 256 x 512 tile by name: its partials do not fit the fixed array, so
+    # it is refused for every shape (also one that would need no partials)
+    for M, N, K in ((0, 16, 24), (8192, 8192, 8192), (4864, 2048, 8192), (300, 520, 200)):
+        assert na(M, N, K, P, max(K, 8), P, max(N, 8), P, max(N, 8), 1.0, 0.0, GEMM_BF16_F32, 4,
+                  0, G.TILE_256x512_2SM, None) == G.GEMM_ERR_SCRATCH
+    # stages 5 and 6 are valid on the noalloc path too (the automatic tile
+    # then holds them); 7 is not
+    assert na(8, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 7, 0, 0,
+              None) == G.GEMM_ERR_ARG
+    assert na(8, 16, 24, P, 24, P, 16, P, 16, 1.0, 0.0, GEMM_BF16_F32, 6, 0, G.TILE_128x256,
+              None) == G.GEMM_ERR_UNSUPPORTED
     assert "fixed array" in lib.gemm_status_string(G.GEMM_ERR_SCRATCH).decode()
 
 
@@ -240,22 +264,13 @@ def test_mma_rate_argument_checks(lib):
     assert lib.mma_rate(16, 4, cyc, None) == G.GEMM_ERR_ARG
 
 
-def test_cublas_comparison_entry_parses_without_a_gpu():
-    import subprocess
-    import sys
-    r = subprocess.run([sys.executable, "-m", "stage_software_pipelining_gb300.vs_cublas", "--help"],
-                       cwd=ROOT, capture_output=True, text=True, timeout=120)
-    assert r.returncode == 0, r.stderr
-    assert "--launches" in r.stdout
-
-
 def test_default_stages_follow_the_tile():
-    # the deepest ring each tile has room for; 3 (valid everywhere) without one
+    # the deepest ring each tile has room for; 4 (valid everywhere) without one
     assert G.default_stages(GEMM_F32) == 2
-    assert G.default_stages(GEMM_BF16_F32) == 3
-    assert G.default_stages(GEMM_BF16_F32, G.TILE_128x128) == 3
+    assert G.default_stages(GEMM_BF16_F32) == 4
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_128x128) == 6
     assert G.default_stages(GEMM_BF16_F32, G.TILE_128x256) == 4
-    assert G.default_stages(GEMM_BF16_F32, G.TILE_256x256_2SM) == 3
+    assert G.default_stages(GEMM_BF16_F32, G.TILE_256x256_2SM) == 6
     assert G.default_stages(GEMM_BF16_F32, G.TILE_256x512_2SM) == 4
 
 

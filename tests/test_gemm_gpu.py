@@ -116,8 +116,7 @@ def test_simt_register_fragment_schemes_agree_bitwise(stages):
 
 # --------------------------------------------------------------------------- tensor cores
 TILES = [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM]
-TILE_STAGES = {G.TILE_128x128: [1, 2, 3], G.TILE_128x256: [1, 2, 3, 4],
-               G.TILE_256x256_2SM: [1, 2, 3], G.TILE_256x512_2SM: [1, 2, 3, 4]}
+TILE_STAGES = {t: list(range(1, G.TILE_MAX_STAGES[t] + 1)) for t in TILES}
 
 
 @pytest.mark.parametrize("dtype", TC_DTYPES)
@@ -151,10 +150,10 @@ def test_tc_shape_fuzz(shape, b_col_major):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("b_col_major", [False, True])
 def test_tc_k_tails_across_the_atoms_of_a_stage(tile, b_col_major):
-    """A stage holds K = 128 as two 64-deep atoms (K = 64 on the 128 x 256
-    tile): K ends inside the first atom, exactly at an atom or stage edge,
-    and inside the second atom, so that one copy of a stage is partly or
-    wholly past K (zero fill).  beta = 1 exercises the C box copies too."""
+    """A stage holds K = 64 (one 128-byte swizzle row of 16-bit data): K ends
+    inside a stage, exactly at a stage edge, and one or two stages past it,
+    so that the last copy of a tile is partly past K (zero fill) and the ring
+    wraps with 2 stages.  beta = 1 exercises the C box copies too."""
     for K in (8, 56, 64, 72, 120, 128, 136, 192, 200, 248, 256, 264):
         inp = make_inputs(workload(GEMM_BF16_F32, 200, 300, K, b_col_major=b_col_major, beta=1.0))
         out, _ = run_gpu(inp, 2, tile=tile)
@@ -261,6 +260,36 @@ def test_automatic_tile_choice_on_gb300():
     assert G.resolve_tile(2048, 2048, 8192, dt) == G.TILE_256x256_2SM
     assert G.resolve_tile(1024, 1024, 4096, dt) == G.TILE_128x128     # 16 pair tiles
     assert G.resolve_tile(8191, 28672, 4096, GEMM_BF16_BF16) == G.TILE_256x256_2SM
+    # rings of 5 or 6 stages take the tile of the same rows per SM that holds them
+    assert G.resolve_tile(8192, 8192, 8192, dt, stages=6) == G.TILE_256x256_2SM
+    assert G.resolve_tile(2048, 2048, 2048, dt, stages=5) == G.TILE_256x256_2SM
+    assert G.resolve_tile(1024, 1024, 4096, dt, stages=6) == G.TILE_128x128
+    assert G.resolve_tile(100, 2048, 512, dt, stages=6) == G.TILE_128x128
+
+
+@pytest.mark.parametrize("dtype", [GEMM_BF16_F32, GEMM_BF16_BF16])
+def test_automatic_six_stage_ring_is_bitwise_the_pair_tile(dtype):
+    """Asking for 6 stages without a tile, where a 4-stage ring would take the
+    256 x 512 tile (which holds 4), runs the 256 x 256 pair tile: the same
+    bits as either tile at any depth, and within the oracle's tolerance."""
+    M, N, K = 2048, 4864, 8192                     # 80 wide tiles on 76 pairs
+    assert G.resolve_tile(M, N, K, dtype, stages=4) == G.TILE_256x512_2SM
+    assert G.resolve_tile(M, N, K, dtype, stages=6) == G.TILE_256x256_2SM
+    w = workload(dtype, M, N, K, beta=0.0)
+    inp = make_inputs(w)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    out_dt = OUT_DTYPE[dtype]
+    outs = {}
+    for key, stages, tile in (("auto6", 6, G.TILE_AUTO), ("pair2", 2, G.TILE_256x256_2SM),
+                              ("wide4", 4, G.TILE_256x512_2SM)):
+        outs[key] = torch.full((M, N), float("nan"), dtype=out_dt, device="cuda")
+        G.gemm(A, B, outs[key], 1.0, 0.0, stages=stages, tile=tile, checked=True)
+    assert torch.equal(outs["auto6"], outs["pair2"])
+    assert torch.equal(outs["auto6"], outs["wide4"])
+    rows, cols = sample_indices(M, N, 600, 11)
+    got = outs["auto6"][torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    ref, absb = oracle.gemm_entries(inp.A, inp.B, None, 1.0, 0.0, rows=rows, cols=cols)
+    check_against_oracle(got.double().cpu().numpy(), ref, absb, dtype, what="auto 6 stages")
 
 
 def test_empty_m_or_n_is_a_noop():
@@ -366,11 +395,12 @@ def sample_indices(M, N, count, seed):
     ("fp16_2048", 3, 0),
     ("bf16_8192_beta1", 4, G.TILE_128x256),
     ("bf16_8192_beta1", 4, G.TILE_256x512_2SM),     # the configuration bench.py times
-    ("bf16_8192_beta1", 3, G.TILE_256x256_2SM),
-    ("bf16_8192_beta1", 3, G.TILE_128x128),
+    ("bf16_8192_beta1", 6, G.TILE_256x256_2SM),
+    ("bf16_8192_beta1", 6, G.TILE_128x128),
+    ("bf16_8192_beta1", 5, 0),                      # automatic tile for a 5-stage ring
     ("bf16_ragged_colB", 4, G.TILE_128x256),
-    ("bf16_ragged_colB", 3, G.TILE_256x256_2SM),
-    ("bf16_ragged_colB", 2, G.TILE_256x256_2SM),
+    ("bf16_ragged_colB", 6, G.TILE_256x256_2SM),     # the configuration bench.py times
+    ("bf16_ragged_colB", 1, G.TILE_256x256_2SM),
     ("bf16_ragged_colB", 4, G.TILE_256x512_2SM),
 ])
 def test_full_size_workload_sampled(name, stages, tile):
@@ -450,7 +480,7 @@ def test_back_to_back_launches_are_deterministic(tile):
 
 
 @pytest.mark.parametrize("M,N,K", [(1_048_581, 136, 40),    # 4097 pair-tile rows, ragged
-                                   (130, 200, 131_080)])    # 1025 stages of K = 128
+                                   (130, 200, 131_080)])    # 2049 stages of K = 64
 def test_extreme_dimensions_sampled(M, N, K):
     """Very tall and very deep problems: tile indices, TMA row coordinates,
     64-bit C offsets and long accumulation chains, checked on sampled

@@ -51,6 +51,8 @@ CASES = [
     ("bf16_8192_beta1", 1100, 904, 4096, G.TILE_256x256_2SM, 3),
     ("bf16_8192_beta1", 700, 1000, 1504, G.TILE_128x256, 3),
     ("bf16_ragged_colB", 1000, 1200, 2048, G.TILE_256x256_2SM, 2),
+    ("bf16_8192_beta1", 1100, 904, 4096, G.TILE_128x128, 6),
+    ("bf16_8192_beta1", 1100, 904, 4096, G.TILE_AUTO, 6),
 ]
 
 
