@@ -41,7 +41,13 @@
  *
  * Memory: A, B and C are device pointers owned by the caller (except in
  * gemm_host, which takes host pointers).  The library keeps no pointer after
- * a call returns.
+ * a call returns.  Two schedules keep fp32 partial tiles in a workspace the
+ * library allocates (cudaMalloc) on first use, one per (device, stream), and
+ * keeps until gemm_host_release: the SIMT path's split tail (used when the
+ * last wave of 128 x 64 tiles -- 3 per SM -- is partial: its tiles are cut
+ * along K into 2..8 pieces; at most 3 x SMs x 32 KB, 14.9 MB on GB300) and
+ * the tensor-core stream-K tail (gemm_schedule_set mode 2).  Every other call
+ * allocates nothing.
  *
  * Alignment (GEMM_ERR_ALIGN otherwise): A, B and C start on 16-byte
  * boundaries and lda*size, ldb*size and ldc*size are multiples of 16 bytes
@@ -186,9 +192,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
               int b_col_major, int tile, void* stream);
 
 /* Frees what the library caches on the current device: gemm_host's staging
- * buffers, copy streams and events, and the stream-K workspaces
- * (gemm_schedule_set mode 2).  Call it when no GEMM of this library is
- * running on the device; later calls create them again as needed. */
+ * buffers, copy streams and events, the SIMT split-tail workspaces and the
+ * stream-K workspaces (gemm_schedule_set mode 2).  Call it when no GEMM of
+ * this library is running on the device; later calls create them again as
+ * needed. */
 int gemm_host_release(void);
 
 /* Human-readable name of a gemm_status_t (static storage). */

@@ -383,6 +383,8 @@ int gemm_host_release(void) {
         }
         host_pipe_release(dev);
     }
+    const int st = ssp::simt_release_workspaces();
+    if (st != GEMM_OK) return st;
     return ssp::tc_release_workspaces();
 }
 
@@ -439,7 +441,7 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int dtype, int stages, int b_col_
         return GEMM_OK;
     }
     if (dtype == GEMM_F32) {
-        if (grid) *grid = static_cast<int>(((M + 127) / 128) * ((N + 63) / 64));
+        if (grid) *grid = ssp::simt_plan(M, N, K, ssp::tc_current_device_sms()).grid;
         if (cluster) *cluster = 1;
         if (smem_bytes) *smem_bytes = stages * (128 * 20 + 16 * 64) * 4;
         return GEMM_OK;

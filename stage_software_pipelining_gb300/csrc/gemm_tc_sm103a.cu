@@ -381,6 +381,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint16_t kPairMask = 0x3;
 
     if (threadIdx.x == 0) {
+        // The tensor maps are kernel parameters, not data an earlier grid
+        // writes: fetch them into the descriptor cache before waiting on it.
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -428,8 +433,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
             const uint32_t stage_bytes = A_STAGE_BYTES + b_stage_bytes;
             // The leader's full[s] counts the bytes of both CTAs of a pair.
             const uint32_t armed_bytes = PAIR ? 2u * stage_bytes : stage_bytes;

@@ -75,6 +75,18 @@ int tc_clear_workspace_flags();
 int tc_read_and_clear_status(GemmDeviceStatus* out);
 
 int simt_launch(const SimtLaunch& L, cudaStream_t stream);
+// Tile schedule of the SIMT kernel for a shape on a GPU with `sms` SMs: tiles
+// [0, dp_tiles) run whole; each later tile (those of a partial last wave) runs
+// as `parts` pieces along K, combined through a workspace of ws_bytes.
+struct SimtPlan {
+    int dp_tiles = 0;
+    int parts = 1;
+    int grid = 0;
+    size_t ws_bytes = 0;
+};
+SimtPlan simt_plan(int64_t M, int64_t N, int64_t K, int sms);
+// Free the split-tail workspaces of the current device.
+int simt_release_workspaces();
 
 // C = beta*C over an M x N block (K == 0 or alpha == 0); elem_bytes 4 (fp32) or 2 (bf16).
 int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,

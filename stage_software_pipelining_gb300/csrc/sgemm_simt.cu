@@ -18,6 +18,17 @@
 // Out-of-range rows/columns are zero-filled by cp.async's source-size operand,
 // so ragged M, N and K need no special path; stores are masked.
 //
+// Tail schedule: the tiles form one wave per 3 CTAs per SM (the occupancy
+// this kernel has at every stage count).  When the last wave is partial, its
+// tiles are cut along K into `parts` equal ranges of K tiles, so that the
+// short pieces fill the SMs the whole tiles leave idle.  Each piece stores
+// its fp32 partial tile in a workspace and counts itself in on the tile's
+// counter; the piece that arrives last adds the partials of parts 0, 1, ...
+// in that order (the same bits whichever piece is last), writes C and resets
+// the counter.  Nothing waits on anything, so no piece can hold up another.
+// The plan depends only on the shape and the SM count, so every stage count
+// gives the same bits.
+//
 // GB300 form of the outer product: the 64 multiply-adds of a k step are 32
 // packed fp32 FMAs (fma.rn.f32x2, sm_100 and later).  Each lane of one is an
 // ordinary fused multiply-add rounded once to nearest, so C is bit-for-bit
@@ -29,7 +40,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/gemm.h"
 #include "internal.h"
@@ -44,6 +57,11 @@ constexpr int A_LD = BK + 4;  // padded row (80 bytes): conflict-free fragment r
 constexpr int A_STAGE_FLOATS = BM * A_LD;
 constexpr int B_STAGE_FLOATS = BK * BN;
 
+constexpr int kSimtCtasPerSm = 3;  // the wave the tail schedule plans for
+constexpr int kSimtMaxParts = 8;
+constexpr int kSimtMinPartKTiles = 4;
+constexpr size_t kSimtCounterBytes = 4096;
+
 struct SimtParams {
     int M, N, K;
     const float* A;
@@ -53,6 +71,11 @@ struct SimtParams {
     float* C;
     long long ldc;
     float alpha, beta;
+    int tiles_n;              // tiles along N
+    int dp_tiles;             // tiles [0, dp_tiles) run whole, one CTA each
+    int parts;                // K pieces of each later tile (1: none)
+    float* ws;                // split tiles: one 128 x 64 fp32 partial per piece
+    unsigned int* counters;   // split tiles: pieces arrived so far
 };
 
 // Copy K tile kt into stage buffers (As, Bs).  A tile: 128 rows x 16 floats =
@@ -103,6 +126,13 @@ __device__ __forceinline__ Pair dup2(float x) {
 // c.lo = fma(a.lo, b.lo, c.lo); c.hi = fma(a.hi, b.hi, c.hi), each rounded once.
 __device__ __forceinline__ void ffma2(Pair& c, Pair a, Pair b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
+}
+
+// Both halves added in fp32, each rounded once.
+__device__ __forceinline__ Pair add2(Pair a, Pair b) {
+    Pair r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 __device__ __forceinline__ float lo32(Pair v) { return __uint_as_float(static_cast<unsigned>(v)); }
@@ -188,53 +218,9 @@ __device__ __forceinline__ void compute_tile(const float* As, const float* Bs, i
     else compute_tile_single(As, Bs, ty, tx, acc);
 }
 
-template <int STAGES, bool FRAG_DB>
-__global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p) {
-    extern __shared__ __align__(16) float smem[];
-    float* As = smem;                              // [STAGES][BM][A_LD]
-    float* Bs = smem + STAGES * A_STAGE_FLOATS;    // [STAGES][BK][BN]
-    const int tid = threadIdx.x;
-    const int ty = tid >> 3, tx = tid & 7;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-    const int KT = (p.K + BK - 1) / BK;
-
-    Pair acc[8][4];  // acc[r][q]: columns 2q, 2q+1 of the thread's 8 (bits of +0.0f: zero)
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[r][q] = 0ull;
-
-    if constexpr (STAGES == 1) {
-        for (int kt = 0; kt < KT; ++kt) {
-            load_tile(p, m0, n0, kt, As, Bs);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncthreads();  // read after write: every thread's copies landed
-            compute_tile<FRAG_DB>(As, Bs, ty, tx, acc);
-            __syncthreads();  // write after read: nobody still reads the buffer
-        }
-    } else {
-#pragma unroll
-        for (int s = 0; s < STAGES - 1; ++s) {
-            if (s < KT) load_tile(p, m0, n0, s, As + s * A_STAGE_FLOATS, Bs + s * B_STAGE_FLOATS);
-            cp_async_commit();  // always commit: a fixed number of groups stays in flight
-        }
-        for (int kt = 0; kt < KT; ++kt) {
-            cp_async_wait<STAGES - 2>();  // this thread's copies of tile kt landed
-            __syncthreads();              // ... everyone's, and slot (kt-1) % S is free
-            const int nk = kt + STAGES - 1;
-            if (nk < KT) {
-                const int ns = nk % STAGES;
-                load_tile(p, m0, n0, nk, As + ns * A_STAGE_FLOATS, Bs + ns * B_STAGE_FLOATS);
-            }
-            cp_async_commit();
-            const int cs = kt % STAGES;
-            compute_tile<FRAG_DB>(As + cs * A_STAGE_FLOATS, Bs + cs * B_STAGE_FLOATS, ty, tx, acc);
-        }
-        cp_async_wait<0>();
-    }
-
-    // Epilogue: C = alpha*acc + beta*C, masked at the M and N edges.
+// C = alpha*acc + beta*C for this thread's 8 x 8 outputs, masked at the M and N edges.
+__device__ __forceinline__ void simt_epilogue(const SimtParams& p, int m0, int n0, int ty, int tx,
+                                              const Pair (&acc)[8][4]) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int gm = m0 + ty + 16 * r;
@@ -273,6 +259,106 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     }
 }
 
+template <int STAGES, bool FRAG_DB>
+__global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p) {
+    extern __shared__ __align__(16) float smem[];
+    float* As = smem;                              // [STAGES][BM][A_LD]
+    float* Bs = smem + STAGES * A_STAGE_FLOATS;    // [STAGES][BK][BN]
+    __shared__ int last_piece;
+    const int tid = threadIdx.x;
+    const int ty = tid >> 3, tx = tid & 7;
+    const int KT = (p.K + BK - 1) / BK;
+    // Whole tile, or piece `part` of a split tile: K tiles [kt0, kt1).
+    int tile = blockIdx.x, part = -1, kt0 = 0, kt1 = KT;
+    if (tile >= p.dp_tiles) {
+        const int u = tile - p.dp_tiles;
+        part = u % p.parts;
+        tile = p.dp_tiles + u / p.parts;
+        kt0 = static_cast<int>(static_cast<long long>(part) * KT / p.parts);
+        kt1 = static_cast<int>(static_cast<long long>(part + 1) * KT / p.parts);
+    }
+    const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
+    const int NK = kt1 - kt0;
+
+    Pair acc[8][4];  // acc[r][q]: columns 2q, 2q+1 of the thread's 8 (bits of +0.0f: zero)
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = 0ull;
+
+    if constexpr (STAGES == 1) {
+        for (int i = 0; i < NK; ++i) {
+            load_tile(p, m0, n0, kt0 + i, As, Bs);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();  // read after write: every thread's copies landed
+            compute_tile<FRAG_DB>(As, Bs, ty, tx, acc);
+            __syncthreads();  // write after read: nobody still reads the buffer
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s) {
+            if (s < NK)
+                load_tile(p, m0, n0, kt0 + s, As + s * A_STAGE_FLOATS, Bs + s * B_STAGE_FLOATS);
+            cp_async_commit();  // always commit: a fixed number of groups stays in flight
+        }
+        for (int i = 0; i < NK; ++i) {
+            cp_async_wait<STAGES - 2>();  // this thread's copies of tile i landed
+            __syncthreads();              // ... everyone's, and slot (i-1) % S is free
+            const int nk = i + STAGES - 1;
+            if (nk < NK) {
+                const int ns = nk % STAGES;
+                load_tile(p, m0, n0, kt0 + nk, As + ns * A_STAGE_FLOATS, Bs + ns * B_STAGE_FLOATS);
+            }
+            cp_async_commit();
+            const int cs = i % STAGES;
+            compute_tile<FRAG_DB>(As + cs * A_STAGE_FLOATS, Bs + cs * B_STAGE_FLOATS, ty, tx, acc);
+        }
+        cp_async_wait<0>();
+    }
+
+    if (part < 0) {
+        simt_epilogue(p, m0, n0, ty, tx, acc);
+        return;
+    }
+    // A piece of a split tile: publish the partial (thread-ordered, so that
+    // each warp access is 512 contiguous bytes), count in, and let the last
+    // piece to arrive finish the tile.
+    const int split = tile - p.dp_tiles;
+    ulonglong2* mine = reinterpret_cast<ulonglong2*>(
+        p.ws + static_cast<size_t>(split * p.parts + part) * (BM * BN));
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        mine[j * THREADS + tid] = make_ulonglong2(acc[j >> 1][(j & 1) * 2], acc[j >> 1][(j & 1) * 2 + 1]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last_piece = atomicAdd(p.counters + split, 1u) == static_cast<unsigned>(p.parts - 1);
+    __syncthreads();
+    if (!last_piece) return;
+    __threadfence();  // the other pieces' partials are visible after their count
+    for (int q = 0; q < p.parts; ++q) {
+        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
+            p.ws + static_cast<size_t>(split * p.parts + q) * (BM * BN));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const ulonglong2 v = __ldcg(src + j * THREADS + tid);  // written by other SMs: read L2
+            Pair& a0 = acc[j >> 1][(j & 1) * 2];
+            Pair& a1 = acc[j >> 1][(j & 1) * 2 + 1];
+            if (q == 0) {
+                a0 = v.x;
+                a1 = v.y;
+            } else {
+                a0 = add2(a0, v.x);
+                a1 = add2(a1, v.y);
+            }
+        }
+    }
+    simt_epilogue(p, m0, n0, ty, tx, acc);
+    if (tid == 0) p.counters[split] = 0u;  // ready for the next launch
+}
+
+int simt_tiles(int M, int N) { return ((M + BM - 1) / BM) * ((N + BN - 1) / BN); }
+
 template <int S, bool FRAG_DB>
 int launch_stages(const SimtParams& p, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(S) * (A_STAGE_FLOATS + B_STAGE_FLOATS) * sizeof(float);
@@ -291,9 +377,34 @@ int launch_stages(const SimtParams& p, cudaStream_t stream) {
             done[dev] = true;
         }
     }
-    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+    const int grid = p.dp_tiles + (simt_tiles(p.M, p.N) - p.dp_tiles) * p.parts;
     sgemm_simt_kernel<S, FRAG_DB><<<grid, THREADS, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}
+
+// Split-tail workspaces, one per (device, stream): launches on one stream are
+// ordered, so they never use a workspace at the same time.  Counters first
+// (zeroed once; every finished tile resets its own), then the partials.
+struct SimtWorkspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_simt_ws_mu;
+std::map<std::pair<int, cudaStream_t>, SimtWorkspace> g_simt_ws;
+
+int simt_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> g(g_simt_ws_mu);
+    SimtWorkspace& w = g_simt_ws[{dev, stream}];
+    if (w.bytes < bytes) {
+        if (w.ptr) cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMemset(w.ptr, 0, kSimtCounterBytes) != cudaSuccess) return GEMM_ERR_CUDA;
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return GEMM_OK;
 }
 
 __global__ void scale_kernel(long long M, long long N, void* C, long long ldc, int out_bf16,
@@ -314,6 +425,28 @@ __global__ void scale_kernel(long long M, long long N, void* C, long long ldc, i
 
 }  // namespace
 
+SimtPlan simt_plan(int64_t M, int64_t N, int64_t K, int sms) {
+    SimtPlan pl;
+    const int T = simt_tiles(static_cast<int>(M), static_cast<int>(N));
+    const int KT = static_cast<int>((K + BK - 1) / BK);
+    const int W = sms * kSimtCtasPerSm;
+    pl.dp_tiles = T;
+    pl.parts = 1;
+    const int R = W > 0 ? T % W : 0;
+    if (W > 0 && T > W && R > 0) {
+        int parts = W / R;
+        if (parts > kSimtMaxParts) parts = kSimtMaxParts;
+        if (parts > KT / kSimtMinPartKTiles) parts = KT / kSimtMinPartKTiles;
+        if (parts >= 2 && R <= static_cast<int>(kSimtCounterBytes / sizeof(unsigned int))) {
+            pl.dp_tiles = T - R;
+            pl.parts = parts;
+            pl.ws_bytes = kSimtCounterBytes + static_cast<size_t>(R) * parts * BM * BN * sizeof(float);
+        }
+    }
+    pl.grid = pl.dp_tiles + (T - pl.dp_tiles) * pl.parts;
+    return pl;
+}
+
 int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
     SimtParams p;
     p.M = static_cast<int>(L.M);
@@ -327,7 +460,25 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
     p.ldc = L.ldc;
     p.alpha = L.alpha;
     p.beta = L.beta;
-    if ((p.M + BM - 1) / BM > 65535) return GEMM_ERR_UNSUPPORTED;
+    p.tiles_n = (p.N + BN - 1) / BN;
+    if (static_cast<long long>(simt_tiles(p.M, p.N)) * kSimtMaxParts > 0x7fffffffLL)
+        return GEMM_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const SimtPlan pl = simt_plan(L.M, L.N, L.K, sms);
+    p.dp_tiles = pl.dp_tiles;
+    p.parts = pl.parts;
+    p.ws = nullptr;
+    p.counters = nullptr;
+    if (pl.ws_bytes) {
+        void* ws = nullptr;
+        const int st = simt_workspace(dev, stream, pl.ws_bytes, &ws);
+        if (st != GEMM_OK) return st;
+        p.counters = static_cast<unsigned int*>(ws);
+        p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSimtCounterBytes);
+    }
     if (L.single_fragments) {
         switch (L.stages) {
             case 1: return launch_stages<1, false>(p, stream);
@@ -344,6 +495,21 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
         case 4: return launch_stages<4, true>(p, stream);
         default: return GEMM_ERR_ARG;
     }
+}
+
+int simt_release_workspaces() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> g(g_simt_ws_mu);
+    for (auto it = g_simt_ws.begin(); it != g_simt_ws.end();) {
+        if (it->first.first == dev) {
+            if (it->second.ptr) cudaFree(it->second.ptr);
+            it = g_simt_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return GEMM_OK;
 }
 
 int scale_launch(int64_t M, int64_t N, void* C, int64_t ldc, int out_bf16, float beta,

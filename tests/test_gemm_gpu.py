@@ -102,6 +102,67 @@ def test_simt_stage_invariance_bitwise():
         assert np.array_equal(o, outs[0]), f"SIMT stages={s} differs from stages=1"
 
 
+def simt_split_plan(M, N, K):
+    """The SIMT kernel's tail schedule, restated from its rule: 3 CTAs per SM
+    make a wave; the tiles of a partial last wave are cut along K into
+    min(8, wave // leftover, K tiles // 4) pieces when that is at least 2."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = -(-M // 128) * -(-N // 64)
+    KT = -(-K // 16)
+    W = 3 * sms
+    R = T % W
+    if T > W and R > 0:
+        parts = min(8, W // R, KT // 4)
+        if parts >= 2:
+            return T - R, parts
+    return T, 1
+
+
+@pytest.mark.parametrize("shape", [(2176, 1792, 256), (2180, 1790, 250), (2048, 2048, 512)])
+def test_simt_split_tail_matches_oracle_and_is_stage_invariant(shape):
+    """Shapes whose last wave of 128 x 64 tiles is partial: those tiles run as
+    K pieces combined through the workspace (also with ragged M, N, K and a
+    K that leaves short pieces).  Every stage count gives the same bits, the
+    bits match a second call, and the result matches the oracle."""
+    M, N, K = shape
+    dp, parts = simt_split_plan(M, N, K)
+    assert parts >= 2, "the shape must exercise the split tail"
+    assert G.plan(M, N, K, GEMM_F32, 2)["grid"] == dp + (-(-M // 128) * -(-N // 64) - dp) * parts
+    inp = make_inputs(workload(GEMM_F32, M, N, K))
+    outs = [run_gpu(inp, s)[0] for s in (1, 2, 3, 4)]
+    again, _ = run_gpu(inp, 2)
+    for s, o in zip((2, 3, 4), outs[1:]):
+        assert np.array_equal(o, outs[0]), f"SIMT split tail: stages={s} differs from stages=1"
+    assert np.array_equal(again, outs[1]), "a second call gives other bits"
+    ref, absb = oracle_full(inp)
+    check_against_oracle(outs[0], ref, absb, GEMM_F32, what=f"simt split tail {shape}")
+
+
+def test_simt_split_tail_alpha_beta_and_streams():
+    """beta != 0 is applied once, by the piece that finishes the tile; two
+    streams at once use two workspaces."""
+    M, N, K = 2176, 1792, 192
+    assert simt_split_plan(M, N, K)[1] >= 2
+    w = workload(GEMM_F32, M, N, K, alpha=-0.5, beta=2.0)
+    inp = make_inputs(w)
+    inp.C0 = torch.rand(M, N, generator=torch.Generator().manual_seed(8)) * 2 - 1
+    A, B = inp.A.cuda(), inp.B.cuda()
+    C1, C2 = inp.C0.cuda(), inp.C0.cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        C1.copy_(inp.C0)
+        C2.copy_(inp.C0)
+        torch.cuda.synchronize()
+        G.gemm(A, B, C1, w.alpha, w.beta, stages=2, stream=s1)
+        G.gemm(A, B, C2, w.alpha, w.beta, stages=3, stream=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(C1, C2)
+    ref, absb = oracle_full(inp)
+    check_against_oracle(C1.double().cpu().numpy(), ref, absb, GEMM_F32, beta=2.0, C0=inp.C0,
+                         what="simt split tail alpha/beta")
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3, 4])
 def test_simt_register_fragment_schemes_agree_bitwise(stages):
     """Double-buffered and single register fragments accumulate in the same
