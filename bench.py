@@ -356,6 +356,12 @@ def run_ours(args):
             pk = sms * 128 * 2 * clocks["sm_mhz"] * 1e-6
             roof["at_sampled_clock"] = {"sm_mhz": clocks["sm_mhz"], "peak": round(pk, 1),
                                         "frac": round(achieved / pk, 4)}
+        if kernel_mhz:
+            # the clock the kernel itself ran at (CTA 0's clock64 over globaltimer)
+            pk = sms * 128 * 2 * kernel_mhz * 1e-6
+            roof["per_clock"] = {"kernel_sm_mhz": round(kernel_mhz, 1),
+                                 "peak_at_kernel_clock": round(pk, 1),
+                                 "frac": round(achieved / pk, 4)}
         roof["model"] = roofline_model(w, flops_step, achieved, peak, peaks)
     else:
         sustained = elapsed_ms > 1000.0

@@ -356,10 +356,11 @@ int gemm_debug_set(int64_t wait_limit_ns, int withhold_arrive);
 
 /*
  * gemm_clock_log -- measurement hook (not thread-safe; affects later launches
- * of the tensor-core kernel from this process).  With dev_buf non-null, CTA 0
- * of every later launch adds, when it exits, its SM clock ticks (clock64) to
- * dev_buf[0] and its wall-clock nanoseconds (globaltimer) to dev_buf[1],
- * both counted from the point where it may first touch global memory.
+ * of the tensor-core and SIMT kernels from this process).  With dev_buf
+ * non-null, CTA 0 of every later launch adds, when it exits, its SM clock
+ * ticks (clock64) to dev_buf[0] and its wall-clock nanoseconds (globaltimer)
+ * to dev_buf[1], both counted from the point where it may first touch global
+ * memory (the SIMT kernel: from the start of its tile).
  * dev_buf[0] * 1000 / dev_buf[1] is then the launches' mean SM clock in MHz.
  *   dev_buf   device pointer to two zeroed 64-bit unsigned integers, owned by
  *             the caller, live until every launch made while it was set has

@@ -154,9 +154,11 @@ ssp::TcLaunch tc_request(int64_t M, int64_t N, int64_t K, const void* A, int64_t
     return L;
 }
 
+// simt_split_from / simt_split_parts: the SIMT tile schedule to use instead
+// of the one planned for these sizes (gemm_host's panels; -1: plan).
 int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
         void* C, int64_t ldc, float alpha, float beta, int dtype, int stages, int b_col_major,
-        int tile, cudaStream_t stream) {
+        int tile, cudaStream_t stream, int simt_split_from = -1, int simt_split_parts = 0) {
     Checked v = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, stages, b_col_major, tile);
     if (v.status != GEMM_OK) return v.status;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -165,7 +167,8 @@ int run(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void*
     if (dtype == GEMM_F32) {
         ssp::SimtLaunch L{M, N, K, static_cast<const float*>(A), lda,
                           static_cast<const float*>(B), ldb, static_cast<float*>(C), ldc,
-                          alpha, beta, stages, tile == GEMM_SIMT_FRAGMENTS_SINGLE};
+                          alpha, beta, stages, tile == GEMM_SIMT_FRAGMENTS_SINGLE, g_clock_log,
+                          simt_split_from, simt_split_parts};
         return ssp::simt_launch(L, stream);
     }
     const ssp::TcLaunch L = tc_request(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
@@ -312,6 +315,10 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
     // panel is a whole number of 256-row tiles.
     const int64_t panel_rows = std::max<int64_t>(256, (M + kHostPanels - 1) / kHostPanels + 255) / 256 * 256;
     const int panels = static_cast<int>((M + panel_rows - 1) / panel_rows);
+    // The SIMT path cuts the tiles of a partial last wave along K: each panel
+    // cuts exactly the tiles the whole call would, so the bits match.
+    const ssp::SimtPlan simt_whole =
+        dtype == GEMM_F32 ? ssp::simt_plan(M, N, K, ssp::tc_current_device_sms()) : ssp::SimtPlan{};
     auto fail = [&]() {
         cudaStreamSynchronize(hp->in);
         cudaStreamSynchronize(s);
@@ -351,8 +358,13 @@ int gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const
         if (ptile == GEMM_TILE_256x512_2SM &&
             resolve_tile(r1 - r0, N, K, GEMM_TILE_AUTO, stages) != GEMM_TILE_256x512_2SM)
             ptile = GEMM_TILE_256x256_2SM;
+        int split_from = -1;
+        if (dtype == GEMM_F32) {
+            const int64_t first_tile = (r0 / 128) * ((N + 63) / 64);
+            split_from = static_cast<int>(std::max<int64_t>(0, simt_whole.dp_tiles - first_tile));
+        }
         st = run(r1 - r0, N, K, need_ab ? pA : hA, lda, need_ab ? dB : B, ldb, pC, ldc, alpha,
-                 beta, dtype, stages, b_col_major, ptile, s);
+                 beta, dtype, stages, b_col_major, ptile, s, split_from, simt_whole.parts);
         if (st != GEMM_OK) {
             fail();
             return st;

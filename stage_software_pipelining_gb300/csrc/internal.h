@@ -47,6 +47,12 @@ struct SimtLaunch {
     float alpha, beta;
     int stages;            // 1..4
     int single_fragments;  // 1: one register fragment set; 0: two (double-buffered)
+    unsigned long long* clock_log;  // device [2] or null: CTA 0's SM clocks and ns
+    // Tile schedule imposed by the caller (gemm_host's row panels follow the
+    // whole call's): split_from < 0 lets simt_launch plan; otherwise tiles
+    // [split_from, ...) of this launch run as split_parts K pieces.
+    int split_from;
+    int split_parts;
 };
 
 // Enqueue the tensor-core GEMM (K > 0, M > 0, N > 0, alpha != 0).  Returns a

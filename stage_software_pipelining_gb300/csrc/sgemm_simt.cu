@@ -76,6 +76,7 @@ struct SimtParams {
     int parts;                // K pieces of each later tile (1: none)
     float* ws;                // split tiles: one 128 x 64 fp32 partial per piece
     unsigned int* counters;   // split tiles: pieces arrived so far
+    unsigned long long* clock_log;  // null, or [2]: CTA 0 adds its SM clocks and ns
 };
 
 // Copy K tile kt into stage buffers (As, Bs).  A tile: 128 rows x 16 floats =
@@ -279,6 +280,14 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     }
     const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
     const int NK = kt1 - kt0;
+    // SM clock of this launch (measurement hook): CTA 0, a whole tile.
+    const bool log_clock = p.clock_log != nullptr && blockIdx.x == 0 && tid == 0;
+    long long clk0 = 0;
+    unsigned long long ns0 = 0;
+    if (log_clock) {
+        clk0 = clock64();
+        ns0 = globaltimer_ns();
+    }
 
     Pair acc[8][4];  // acc[r][q]: columns 2q, 2q+1 of the thread's 8 (bits of +0.0f: zero)
 #pragma unroll
@@ -319,6 +328,10 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
 
     if (part < 0) {
         simt_epilogue(p, m0, n0, ty, tx, acc);
+        if (log_clock) {
+            atomicAdd(p.clock_log, static_cast<unsigned long long>(clock64() - clk0));
+            atomicAdd(p.clock_log + 1, globaltimer_ns() - ns0);
+        }
         return;
     }
     // A piece of a split tile: publish the partial (thread-ordered, so that
@@ -427,7 +440,9 @@ __global__ void scale_kernel(long long M, long long N, void* C, long long ldc, i
 
 SimtPlan simt_plan(int64_t M, int64_t N, int64_t K, int sms) {
     SimtPlan pl;
-    const int T = simt_tiles(static_cast<int>(M), static_cast<int>(N));
+    const long long T64 = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    if (T64 * kSimtMaxParts > 0x7fffffffLL) return pl;  // too many tiles: simt_launch refuses
+    const int T = static_cast<int>(T64);
     const int KT = static_cast<int>((K + BK - 1) / BK);
     const int W = sms * kSimtCtasPerSm;
     pl.dp_tiles = T;
@@ -461,17 +476,35 @@ int simt_launch(const SimtLaunch& L, cudaStream_t stream) {
     p.alpha = L.alpha;
     p.beta = L.beta;
     p.tiles_n = (p.N + BN - 1) / BN;
-    if (static_cast<long long>(simt_tiles(p.M, p.N)) * kSimtMaxParts > 0x7fffffffLL)
+    // The grid is 1-D: tiles (and their pieces) must number below 2^31.
+    if (((L.M + BM - 1) / BM) * ((L.N + BN - 1) / BN) * kSimtMaxParts > 0x7fffffffLL)
         return GEMM_ERR_UNSUPPORTED;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return GEMM_ERR_CUDA;
-    const SimtPlan pl = simt_plan(L.M, L.N, L.K, sms);
+    SimtPlan pl = simt_plan(L.M, L.N, L.K, sms);
+    if (L.split_from >= 0) {
+        // The caller's schedule: the same pieces a larger call would cut.
+        const int T = simt_tiles(p.M, p.N);
+        pl.dp_tiles = L.split_from < T ? L.split_from : T;
+        pl.parts = pl.dp_tiles < T ? L.split_parts : 1;
+        if (pl.parts < 2) {
+            pl.dp_tiles = T;
+            pl.parts = 1;
+        }
+        if (T - pl.dp_tiles > static_cast<int>(kSimtCounterBytes / sizeof(unsigned int)))
+            return GEMM_ERR_UNSUPPORTED;
+        pl.ws_bytes = pl.parts > 1 ? kSimtCounterBytes + static_cast<size_t>(T - pl.dp_tiles) *
+                                                             pl.parts * BM * BN * sizeof(float)
+                                   : 0;
+        pl.grid = pl.dp_tiles + (T - pl.dp_tiles) * pl.parts;
+    }
     p.dp_tiles = pl.dp_tiles;
     p.parts = pl.parts;
     p.ws = nullptr;
     p.counters = nullptr;
+    p.clock_log = L.clock_log;
     if (pl.ws_bytes) {
         void* ws = nullptr;
         const int st = simt_workspace(dev, stream, pl.ws_bytes, &ws);

@@ -59,11 +59,15 @@ def test_rejects_more_ctas_than_sms():
         G.mma_rate(n_mma=16, ctas=sms + 1)
 
 
-@pytest.mark.parametrize("tile", [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM])
+@pytest.mark.parametrize("tile", [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM,
+                                  G.TILE_256x512_2SM, "simt"])
 def test_clock_log_of_the_gemm(tile):
     gen = torch.Generator().manual_seed(7)
-    A = (torch.rand(2048, 2048, generator=gen) - 0.5).to(torch.bfloat16).cuda()
-    B = (torch.rand(2048, 2048, generator=gen) - 0.5).to(torch.bfloat16).cuda()
+    dt = torch.float32 if tile == "simt" else torch.bfloat16
+    A = (torch.rand(2048, 2048, generator=gen) - 0.5).to(dt).cuda()
+    B = (torch.rand(2048, 2048, generator=gen) - 0.5).to(dt).cuda()
+    if tile == "simt":
+        tile = G.SIMT_FRAGMENTS_DOUBLE
     C = torch.zeros(2048, 2048, device="cuda")
     log = torch.zeros(2, dtype=torch.int64, device="cuda")
     G.clock_log(log)
