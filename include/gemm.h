@@ -47,7 +47,9 @@
  * last wave of 128 x 64 tiles -- 3 per SM -- is partial: its tiles are cut
  * along K into 2..8 pieces; at most 3 x SMs x 32 KB, 14.9 MB on GB300) and
  * the tensor-core stream-K tail (gemm_schedule_set mode 2).  Every other call
- * allocates nothing.
+ * allocates nothing.  A call that would allocate cannot run inside a stream
+ * capture: make the first such call on each (device, stream) before capturing
+ * (a larger shape later may grow the workspace again).
  *
  * Alignment (GEMM_ERR_ALIGN otherwise): A, B and C start on 16-byte
  * boundaries and lda*size, ldb*size and ldc*size are multiples of 16 bytes
