@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     }
     const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
     const int NK = kt1 - kt0;
-    // SM clock of this launch (measurement hook): CTA 0, a whole tile.
+    // SM clock of this launch (measurement hook): CTA 0, from here to its exit.
     const bool log_clock = p.clock_log != nullptr && blockIdx.x == 0 && tid == 0;
     long long clk0 = 0;
     unsigned long long ns0 = 0;
@@ -288,6 +288,12 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
         clk0 = clock64();
         ns0 = globaltimer_ns();
     }
+    auto log_exit = [&]() {
+        if (log_clock) {
+            atomicAdd(p.clock_log, static_cast<unsigned long long>(clock64() - clk0));
+            atomicAdd(p.clock_log + 1, globaltimer_ns() - ns0);
+        }
+    };
 
     Pair acc[8][4];  // acc[r][q]: columns 2q, 2q+1 of the thread's 8 (bits of +0.0f: zero)
 #pragma unroll
@@ -328,10 +334,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
 
     if (part < 0) {
         simt_epilogue(p, m0, n0, ty, tx, acc);
-        if (log_clock) {
-            atomicAdd(p.clock_log, static_cast<unsigned long long>(clock64() - clk0));
-            atomicAdd(p.clock_log + 1, globaltimer_ns() - ns0);
-        }
+        log_exit();
         return;
     }
     // A piece of a split tile: publish the partial (thread-ordered, so that
@@ -347,7 +350,10 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     __syncthreads();
     if (tid == 0) last_piece = atomicAdd(p.counters + split, 1u) == static_cast<unsigned>(p.parts - 1);
     __syncthreads();
-    if (!last_piece) return;
+    if (!last_piece) {
+        log_exit();
+        return;
+    }
     __threadfence();  // the other pieces' partials are visible after their count
     for (int q = 0; q < p.parts; ++q) {
         const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
@@ -368,6 +374,7 @@ __global__ void __launch_bounds__(THREADS) sgemm_simt_kernel(const SimtParams p)
     }
     simt_epilogue(p, m0, n0, ty, tx, acc);
     if (tid == 0) p.counters[split] = 0u;  // ready for the next launch
+    log_exit();
 }
 
 int simt_tiles(int M, int N) { return ((M + BM - 1) / BM) * ((N + BN - 1) / BN); }
