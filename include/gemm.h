@@ -125,7 +125,7 @@ typedef enum {
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_ARG = -1,          /* bad size, leading dimension, pointer, dtype or stages */
-    GEMM_ERR_UNSUPPORTED = -2,  /* a valid request this build does not implement */
+    GEMM_ERR_UNSUPPORTED = -2,  /* a valid request the library does not implement */
     GEMM_ERR_ALIGN = -3,        /* a 16-byte alignment rule above is broken */
     GEMM_ERR_LAUNCH = -4,       /* the CUDA launch (or tensor-map encode) failed */
     GEMM_ERR_TIMEOUT = -5,      /* a pipeline wait ran out (gemm_checked only) */

@@ -72,7 +72,7 @@ def test_bad_dtype_and_stages(lib):
     # every stage is a K slice of 64: shared memory holds 6 stages for the
     # 128 x 128 and 256 x 256 pair tiles and 4 for the 128 x 256 and 256 x 512
     # tiles; 1..6 is the valid range, a deeper ring than an explicit tile
-    # holds is a valid request this build does not implement
+    # holds is a valid request the library does not implement
     for bad in (0, 7, 8, -1):
         for t in (0, G.TILE_128x128, G.TILE_256x256_2SM):
             assert gemm_ex(lib, 8, 512, 8, stages=bad, tile=t) == G.GEMM_ERR_ARG
