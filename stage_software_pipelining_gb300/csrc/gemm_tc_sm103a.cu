@@ -31,8 +31,9 @@
 //     stream overlap their prologue through programmatic dependent launch.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
-// TMEM owner (the whole warp on one-CTA tiles, lane 0 of the leader on a CTA
-// pair), warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)...).
+// TMEM owner (the whole warp with an elected issuing lane; lane 0 of the
+// leader alone on the 256 x 512 tile), warps 2..5 = epilogue (warp w reads
+// TMEM lanes 32*(w%4)...).
 //
 // Ring protocol (slot s = i mod S, n = i div S for the i-th K tile a CTA
 // handles): the producer waits empty[s] for parity (n&1)^1, arms full[s] with
@@ -539,15 +540,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // On a one-CTA tile the whole warp runs the issue loop: every lane
-        // polls the ring's barriers and elect.sync picks the lane that issues
-        // each MMA and commit.  A lone issuing lane that stops for a barrier
-        // poll every 4 MMAs leaves the tensor pipe idle for part of the poll;
-        // the convergent warp does not (measured: +6.5 % on the 128 x 128 tile
-        // at 6 stages, +1.5 % on the 128 x 256 tile of fp16 2048^3, the same
-        // bits).  A CTA pair keeps the leader's lane 0 alone, which measured
-        // level or better there.
-        if ((!PAIR || lane == 0) && leader) {
+        // With 4 MMAs per stage the whole warp runs the issue loop (on a CTA
+        // pair, the leader's warp): every lane polls the ring's barriers and
+        // elect.sync picks the lane that issues each MMA and commit.  A lone
+        // issuing lane that stops for a barrier poll every 4 MMAs leaves the
+        // tensor pipe idle for part of the poll; the convergent warp does not
+        // (measured, the same bits: +6.5 % on the 128 x 128 tile at 6 stages,
+        // +1.5 % on the 128 x 256 tile of fp16 2048^3, +1 to 2 % on the
+        // 256 x 256 pair tile).  The 256 x 512 tile, with 8 MMAs per stage and
+        // the held-back second half, keeps the leader's lane 0 alone, which
+        // measured level or better there.
+        if ((!WIDE || lane == 0) && leader) {
             // -------------------------------------------------------- MMA issuer
             // K-major operands: 128-byte rows (the stage's K = 64), 8-row groups
             // 1024 bytes apart; one K=16 step is 32 bytes along the row.
@@ -572,12 +575,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int lt = 0;
             bool ok = true;
             Job job;
-            // A bounded ring wait; on a one-CTA tile every lane waits and the
-            // warp goes on only if all of them saw the phase complete.
+            // A bounded ring wait; in the convergent loop every lane waits and
+            // the warp goes on only if all of them saw the phase complete.
             auto mma_wait = [&](uint32_t bar, uint32_t parity, int itx) -> bool {
                 const bool r = bounded_wait<PAIR>(bar, parity, abort_flag, p.wait_limit_ns, ROLE_MMA,
                                                   itx, peer_rank);
-                if constexpr (PAIR) return r;
+                if constexpr (WIDE) return r;
                 else return __all_sync(0xffffffffu, r) != 0;
             };
             if constexpr (WIDE) {
@@ -693,18 +696,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd = (static_cast<uint64_t>(b_hi) << 32) |
                                             (b_s + static_cast<uint32_t>(kk) * b_k16);
                         const uint32_t accum = (kt != job.kb || kk != 0) ? 1u : 0u;
-                        if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
-                        else {
-                            if (elect_one_sync()) umma_f16(d_tmem, ad, bd, p.idesc, accum);
-                            __syncwarp();
+                        if (elect_one_sync()) {
+                            if constexpr (PAIR) umma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
+                            else umma_f16(d_tmem, ad, bd, p.idesc, accum);
                         }
-                    }
-                    // slot s is free (in both CTAs) once these MMAs finish
-                    if constexpr (PAIR) umma_commit_pair_multicast(empty_bar(s), kPairMask);
-                    else {
-                        if (elect_one_sync()) umma_commit(empty_bar(s));
                         __syncwarp();
                     }
+                    // slot s is free (in both CTAs) once these MMAs finish
+                    if (elect_one_sync()) {
+                        if constexpr (PAIR) umma_commit_pair_multicast(empty_bar(s), kPairMask);
+                        else umma_commit(empty_bar(s));
+                    }
+                    __syncwarp();
                     ++it;
                     if (++s == S) {
                         s = 0;
@@ -713,18 +716,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 // accumulator ready for the epilogue (of both CTAs)
-                if constexpr (PAIR) umma_commit_pair_multicast(tfull_bar(acc), kPairMask);
-                else {
-                    if (elect_one_sync()) umma_commit(tfull_bar(acc));
-                    __syncwarp();
+                if (elect_one_sync()) {
+                    if constexpr (PAIR) umma_commit_pair_multicast(tfull_bar(acc), kPairMask);
+                    else umma_commit(tfull_bar(acc));
                 }
+                __syncwarp();
             }
             }
             if (!ok) {
-                // Wait for every MMA this thread issued before TMEM is freed.
-                if constexpr (PAIR) umma_commit_pair_multicast(drain_bar, 0x1);
+                // Wait for every MMA this warp issued before TMEM is freed.
+                if constexpr (WIDE) umma_commit_pair_multicast(drain_bar, 0x1);
                 else {
-                    if (elect_one_sync()) umma_commit(drain_bar);
+                    if (elect_one_sync()) {
+                        if constexpr (PAIR) umma_commit_pair_multicast(drain_bar, 0x1);
+                        else umma_commit(drain_bar);
+                    }
                     __syncwarp();
                 }
                 if (lane == 0) drain_wait(drain_bar, 0u, p.wait_limit_ns);
