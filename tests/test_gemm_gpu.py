@@ -360,7 +360,8 @@ def test_empty_m_or_n_is_a_noop():
 
 
 # --------------------------------------------------------------------------- fault path
-@pytest.mark.parametrize("tile", [G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM])
+@pytest.mark.parametrize("tile", [G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM,
+                                  G.TILE_256x512_2SM])
 def test_withheld_arrive_times_out_and_context_survives(tile):
     """Block 0's producer skips one stage: the MMA wait must run out, the
     kernel must return GEMM_ERR_TIMEOUT (no hang, no trap), and the next
