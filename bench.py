@@ -416,7 +416,7 @@ def run_ours(args):
             "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
                        "alpha": w.alpha, "beta": w.beta, "stages": stages,
                        "schedule": SCHEDULE_NAMES[args.schedule],
-                       "tile": "128x64x16 (SIMT)" if w.dtype == GEMM_F32
+                       "tile": "128x64x32 (SIMT)" if w.dtype == GEMM_F32
                        else TILE_NAMES[tile], "b_layout": "col" if w.b_col_major else "row",
                        "l2": f"inputs larger than L2 ({algorithmic_bytes(w) / 1e6:.0f} MB "
                              f"touched per step > 129 MB); no flush",

@@ -142,7 +142,7 @@ typedef enum {
  *              beta != 0 and written
  *   dtype      a gemm_dtype_t
  *   stages     depth of the shared-memory ring, each stage a K slice of 64:
- *              1..6 on the tensor-core path, 1..4 on the SIMT path (16 of K
+ *              1..6 on the tensor-core path, 1..4 on the SIMT path (32 of K
  *              per stage); anything else is GEMM_ERR_ARG
  *   stream     cudaStream_t
  * The tensor-core tile is GEMM_TILE_AUTO's choice for these sizes and this

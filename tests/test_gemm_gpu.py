@@ -105,14 +105,15 @@ def test_simt_stage_invariance_bitwise():
 def simt_split_plan(M, N, K):
     """The SIMT kernel's tail schedule, restated from its rule: 3 CTAs per SM
     make a wave; the tiles of a partial last wave are cut along K into
-    min(8, wave // leftover, K tiles // 4) pieces when that is at least 2."""
+    min(8, wave // leftover, K tiles of 32 // 2) pieces when that is at
+    least 2 (a piece spans at least 64 of K)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     T = -(-M // 128) * -(-N // 64)
-    KT = -(-K // 16)
+    KT = -(-K // 32)
     W = 3 * sms
     R = T % W
     if T > W and R > 0:
-        parts = min(8, W // R, KT // 4)
+        parts = min(8, W // R, KT // 2)
         if parts >= 2:
             return T - R, parts
     return T, 1
