@@ -9,7 +9,7 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
-    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a); runs on the GPU box")
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
 
 
 def cuda_available() -> bool:
