@@ -1265,10 +1265,16 @@ int plan(const TcLaunch& L, TcParams& p, Geometry& geo) {
     geo.wide = wide;
     p.k_tiles = static_cast<int>((L.K + BK - 1) / BK);
     // Tile rows per raster group.  The tiles running at once should touch as
-    // few A rows and B columns as possible: on the 256 x 512 tile a round of
-    // 76 pairs spans about 12 rows and 6 columns of tiles (measured: 4 %
-    // fewer DRAM bytes than groups of 8, and level or slightly faster).
-    p.group_m = pair ? (wide ? 12 : 8) : 16;
+    // few A rows and B columns as possible, and a group's A panel should stay
+    // in L2 while the group walks its columns.  On the 256 x 512 tile a round
+    // of 76 pairs spans about 12 rows and 6 columns of tiles (measured: 4 %
+    // fewer DRAM bytes than groups of 8, and level or slightly faster).  On
+    // the 256 x 256 tile the group holds about 32 MB of A: 16 tile rows at
+    // K = 4096 (+1.7 % in long runs on 8191 x 28672 x 4096 against 8), 8 at
+    // K = 8192 (16 lost 2 % there).
+    int pair_group = static_cast<int>((32ll << 20) / (2ll * tile_m * (L.K > 0 ? L.K : 1)));
+    pair_group = pair_group < 8 ? 8 : (pair_group > 16 ? 16 : pair_group);
+    p.group_m = pair ? (wide ? 12 : pair_group) : 16;
     p.stages = S;
     p.bn = bn;
     p.b_mn_major = L.b_col_major ? 0 : 1;
