@@ -47,6 +47,8 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "bf16_8192_beta1"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_bf16_8192_traffic.txt")
+SWEEP_PAUSE_S = 0.25   # idle time before each stage-sweep entry
+
 KERNEL_SOURCES = ["stage_software_pipelining_gb300/csrc/gemm_tc_sm103a.cu",
                   "stage_software_pipelining_gb300/csrc/ptx.cuh"]
 
@@ -274,12 +276,15 @@ def run_ours(args):
     flops_step = w.flops
     value = whole_job_rate(flops_step, args.steps, world, elapsed_ms * 1e-3) / 1e12
 
-    # the stage sweep (same workload, same launch stream)
+    # the stage sweep (same workload, same launch stream).  Each entry starts
+    # after a short idle pause, so that no entry inherits the power state (and
+    # clock) that the entries before it left behind.
     sweep = []
     if not args.no_sweep and w.dtype != GEMM_F32:
         for tn in (G.TILE_128x128, G.TILE_128x256, G.TILE_256x256_2SM, G.TILE_256x512_2SM):
             for s in range(1, TILE_MAX_STAGES[tn] + 1):
                 reps = max(10, min(200, args.steps // 10))
+                time.sleep(SWEEP_PAUSE_S)
                 for _ in range(3):
                     step(s, tn)
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -298,6 +303,7 @@ def run_ours(args):
                                 (G.SIMT_FRAGMENTS_SINGLE, "single register fragments")):
             for s in (1, 2, 3, 4):
                 reps = max(10, min(200, args.steps // 10))
+                time.sleep(SWEEP_PAUSE_S)
                 for _ in range(3):
                     step(s, frag)
                 e0 = torch.cuda.Event(enable_timing=True)
