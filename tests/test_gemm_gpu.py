@@ -112,7 +112,7 @@ def simt_split_plan(M, N, K):
     KT = -(-K // 32)
     W = 3 * sms
     R = T % W
-    if T > W and R > 0:
+    if R > 0:
         parts = min(8, W // R, KT // 2)
         if parts >= 2:
             return T - R, parts
