@@ -44,8 +44,9 @@
  * a call returns.  Two schedules keep fp32 partial tiles in a workspace the
  * library allocates (cudaMalloc) on first use, one per (device, stream), and
  * keeps until gemm_host_release: the SIMT path's split tail (used when the
- * last wave of 128 x 64 tiles -- 3 per SM -- is partial: its tiles are cut
- * along K into 2..8 pieces; at most 3 x SMs x 32 KB, 14.9 MB on GB300) and
+ * last wave of 128 x 64 tiles -- 3 per SM -- is partial, also when it is the
+ * only one: its tiles are cut along K into 2..8 pieces; at most 3 x SMs x
+ * 32 KB, 14.9 MB on GB300) and
  * the tensor-core stream-K tail (gemm_schedule_set mode 2).  Every other call
  * allocates nothing.  A call that would allocate cannot run inside a stream
  * capture: make the first such call on each (device, stream) before capturing
